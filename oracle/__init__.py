@@ -1,0 +1,228 @@
+"""Oracle for the blockwise quantize / pack / dequantize / reduce path.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE. Only the test suite, the package smoke
+check and the benchmark's CPU-baseline leg may import this package. The
+product library never loads it, and this package never loads the product.
+
+The arithmetic lives in ``zq_oracle.c`` (plain single-threaded C, compiled
+with ``-O2 -ffp-contract=off`` so that every binary32 operation is rounded
+once, as written). This module only compiles it, loads it with ctypes and
+marshals numpy arrays. Parity status of every function is stated in
+``zq_oracle.c``'s header and in the tests that pin it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "zq_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD_DIR, "libzq_oracle.so")
+
+# gcc flags: IEEE binary32 arithmetic with no contraction into FMA and no
+# value-changing optimisations; the same flags on x86-64 and aarch64.
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-Wall"]
+
+F32, F16, BF16 = 0, 1, 2
+INT2, INT4, INT6, INT8, E4M3 = 2, 4, 6, 8, 0x48
+BITS = {INT2: 2, INT4: 4, INT6: 6, INT8: 8, E4M3: 8}
+
+# Outputs are pre-filled with this byte (and scales with NaN) so that a byte
+# the oracle forgets to write shows up in the checks.
+GARBAGE = 0xA5
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(src: str = _SRC, out: str = _LIB, extra_flags=()) -> str:
+    """Compile ``src`` into the shared library ``out`` with gcc; return ``out``."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    cmd = ["gcc", *CFLAGS, *extra_flags, "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    return out
+
+
+def _stale() -> bool:
+    return not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+
+
+def _declare(lib):
+    i64, i32, u32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_uint32, ctypes.c_void_p
+    lib.orc_codes_bytes.argtypes = [i32, i64]
+    lib.orc_codes_bytes.restype = i64
+    lib.orc_num_blocks.argtypes = [i64, i64]
+    lib.orc_num_blocks.restype = i64
+    for name in ("orc_f16_decode", "orc_bf16_decode", "orc_e4m3_decode"):
+        getattr(lib, name).argtypes = [u32]
+        getattr(lib, name).restype = ctypes.c_float
+    for name in ("orc_f16_encode", "orc_bf16_encode", "orc_e4m3_encode"):
+        getattr(lib, name).argtypes = [ctypes.c_float]
+        getattr(lib, name).restype = u32
+    lib.orc_quantize.argtypes = [vp, i32, i64, i32, i64, vp, vp]
+    lib.orc_dequantize.argtypes = [vp, vp, i64, i32, i64, vp, i32]
+    lib.orc_reduce.argtypes = [vp, vp, i32, i64, i32, i64, vp, vp, i32, i64, vp]
+    lib.orc_fp8_accumulate.argtypes = [vp, vp, vp, i32, i64, i64]
+    lib.orc_encode_n.argtypes = [i32, vp, i64, vp]
+    lib.orc_decode_n.argtypes = [i32, vp, i64, vp]
+    lib.orc_encode_n.restype = i32
+    lib.orc_decode_n.restype = i32
+    for name in ("orc_quantize", "orc_dequantize", "orc_reduce", "orc_fp8_accumulate"):
+        getattr(lib, name).restype = i32
+    return lib
+
+
+def load(path: str | None = None):
+    """Load the compiled oracle (building it first if it is missing or stale)."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            if _stale():
+                build()
+            _lib = _declare(ctypes.CDLL(_LIB))
+    return _lib
+
+
+# ---------------------------------------------------------------------------
+# numpy conveniences. 16-bit floats travel as uint16 bit patterns (bf16 has no
+# numpy dtype); fp16 arrays may also be passed as np.float16.
+# ---------------------------------------------------------------------------
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def _dtype_code(a: np.ndarray, dtype: int | None) -> int:
+    if dtype is not None:
+        return dtype
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.float16:
+        return F16
+    raise ValueError("pass dtype= for uint16 (bf16/f16) bit patterns")
+
+
+def codes_bytes(fmt: int, n: int, lib=None) -> int:
+    return int((lib or load()).orc_codes_bytes(fmt, n))
+
+
+def num_blocks(n: int, G: int, lib=None) -> int:
+    return int((lib or load()).orc_num_blocks(n, G))
+
+
+def quantize(x: np.ndarray, fmt: int, G: int, dtype: int | None = None, lib=None):
+    """Return (codes uint8[codes_bytes], scales float32[num_blocks])."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x)
+    n = x.size
+    codes = np.full(codes_bytes(fmt, n, lib), GARBAGE, dtype=np.uint8)
+    scales = np.full(max(num_blocks(n, G, lib), 0), np.nan, dtype=np.float32)
+    rc = lib.orc_quantize(_ptr(x), _dtype_code(x, dtype), n, fmt, G, _ptr(codes), _ptr(scales))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return codes, scales
+
+
+_OUT_NP = {F32: np.float32, F16: np.uint16, BF16: np.uint16}
+
+
+def dequantize(codes: np.ndarray, scales: np.ndarray, n: int, fmt: int, G: int, out_dtype: int,
+               lib=None) -> np.ndarray:
+    """Return the dequantized values (float32, or uint16 bit patterns for f16/bf16)."""
+    lib = lib or load()
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    out = np.full(n * np.dtype(_OUT_NP[out_dtype]).itemsize, GARBAGE, np.uint8).view(_OUT_NP[out_dtype])
+    rc = lib.orc_dequantize(_ptr(codes), _ptr(scales), n, fmt, G, _ptr(out), out_dtype)
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out
+
+
+def reduce(codes_list, scales_list, n: int, fmt_in: int, G_in: int, fmt_out: int, G_out: int,
+           want_sum: bool = False, lib=None):
+    """Return (codes, scales, sum_or_None) of the shard-ordered quantized reduce."""
+    lib = lib or load()
+    codes_list = [np.ascontiguousarray(c, dtype=np.uint8) for c in codes_list]
+    scales_list = [np.ascontiguousarray(s, dtype=np.float32) for s in scales_list]
+    N = len(codes_list)
+    cp = (ctypes.c_void_p * N)(*[_ptr(c) for c in codes_list])
+    sp = (ctypes.c_void_p * N)(*[_ptr(s) for s in scales_list])
+    out_codes = np.full(codes_bytes(fmt_out, n, lib), GARBAGE, dtype=np.uint8)
+    out_scales = np.full(max(num_blocks(n, G_out, lib), 0), np.nan, dtype=np.float32)
+    sum_out = np.full(n, np.nan, dtype=np.float32) if want_sum else None
+    rc = lib.orc_reduce(ctypes.addressof(cp), ctypes.addressof(sp), N, n, fmt_in, G_in,
+                        _ptr(out_codes), _ptr(out_scales), fmt_out, G_out,
+                        _ptr(sum_out) if want_sum else None)
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out_codes, out_scales, sum_out
+
+
+def fp8_accumulate(codes: np.ndarray, scales: np.ndarray, grad: np.ndarray, G: int,
+                   grad_dtype: int | None = None, lib=None):
+    """Return new (codes, scales) after one in-place FP8 accumulate step (inputs untouched)."""
+    lib = lib or load()
+    codes = np.array(codes, dtype=np.uint8, copy=True)
+    scales = np.array(scales, dtype=np.float32, copy=True)
+    grad = np.ascontiguousarray(grad)
+    rc = lib.orc_fp8_accumulate(_ptr(codes), _ptr(scales), _ptr(grad),
+                                _dtype_code(grad, grad_dtype), grad.size, G)
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return codes, scales
+
+
+_KIND = {"f16": F16, "bf16": BF16, "e4m3": E4M3}
+
+
+def encode_array(kind: str, x: np.ndarray, lib=None) -> np.ndarray:
+    """Round float32 values to f16 / bf16 / e4m3 bit patterns (uint32 array)."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.zeros(x.size, dtype=np.uint32)
+    if lib.orc_encode_n(_KIND[kind], _ptr(x), x.size, _ptr(out)) != 0:
+        raise ValueError(kind)
+    return out
+
+
+def decode_array(kind: str, c: np.ndarray, lib=None) -> np.ndarray:
+    """Decode f16 / bf16 / e4m3 bit patterns to float32."""
+    lib = lib or load()
+    c = np.ascontiguousarray(c, dtype=np.uint32)
+    out = np.zeros(c.size, dtype=np.float32)
+    if lib.orc_decode_n(_KIND[kind], _ptr(c), c.size, _ptr(out)) != 0:
+        raise ValueError(kind)
+    return out
+
+
+def e4m3_decode(c: int, lib=None) -> float:
+    return float((lib or load()).orc_e4m3_decode(c))
+
+
+def e4m3_encode(x: float, lib=None) -> int:
+    return int((lib or load()).orc_e4m3_encode(x))
+
+
+def f16_decode(h: int, lib=None) -> float:
+    return float((lib or load()).orc_f16_decode(h))
+
+
+def f16_encode(x: float, lib=None) -> int:
+    return int((lib or load()).orc_f16_encode(x))
+
+
+def bf16_decode(h: int, lib=None) -> float:
+    return float((lib or load()).orc_bf16_decode(h))
+
+
+def bf16_encode(x: float, lib=None) -> int:
+    return int((lib or load()).orc_bf16_encode(x))

@@ -1,0 +1,431 @@
+/*
+ * zq_oracle.c -- the oracle for the blockwise quantize / pack / dequantize /
+ * quantized-reduce / FP8-accumulate path.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE. This is a plain, slow, single-threaded
+ * restatement of what the path computes, written so that it can be checked
+ * against the pages by eye. Only the test suite, the package smoke check and
+ * the benchmark's CPU-baseline leg may load it. It shares no source, header,
+ * table or helper with the CUDA library, and it never calls it.
+ *
+ * What the pages fix (titles and sections of the source pages):
+ *  [ZeRO++]  "Quantized LLM Training at Scale with ZeRO++", section "Blockwise
+ *            weight quantization cuts forward-gather traffic in half": weights
+ *            are split into blocks and each block is quantized to 8 bits with
+ *            its own scale.  Section "QGZ keeps reductions in full precision
+ *            while sending quantized gradients": 4- or 8-bit gradients are
+ *            dequantized and summed in full precision, then requantized once.
+ *  [Aquavit] "Aquavit: Ascending Quantization for Communication-Efficient
+ *            Vast-Scale Distributed Training" (review), summary item on
+ *            granularity modulation and the glossary entry (Eq. 6, Table 1):
+ *            b stays in {2,4,6,8}, each G-element block carries 32 bits of
+ *            metadata, so the effective width is b + 32/G bits per element.
+ *  [AGoQ]    "AGoQ: Activation and Gradient Quantization for Memory-Efficient
+ *            Distributed Training of LLMs", section 2.B (QuanGrad), "Local
+ *            Accumulation" (dequantize the FP8 main gradient, add the new
+ *            gradient, requantize) and "Precision-Preserved All-Reduce", step
+ *            2 "Local Reduce" (dequantize to FP32, sum, requantize to FP8).
+ *
+ * Readings taken where the pages are silent (each one is a choice):
+ *  R1  symmetric codes with one fp32 scale per block and no zero point
+ *      (the 32 metadata bits of [Aquavit] are that scale);
+ *  R2  scale = absmax / (2^(b-1) - 1) for integer codes and absmax / 448 for
+ *      E4M3 (448 is the largest finite E4M3 value);
+ *  R3  every rounding is IEEE round-to-nearest, ties-to-even: the division,
+ *      the rounding to an integer code and every format conversion;
+ *  R4  x / s is one IEEE binary32 division; no fused multiply-add anywhere
+ *      (this file must be compiled with -ffp-contract=off);
+ *  R5  integer codes are b-bit two's complement in [-qmax, qmax], packed
+ *      LSB-first into a bit stream (bit j of the stream is bit j%8 of byte
+ *      j/8, i.e. a little-endian stream of 32-bit words); the stream is zero
+ *      padded to a multiple of 4 bytes; E4M3 codes are one byte each; scales
+ *      are a separate fp32 array in block order;
+ *  R6  blocks are G consecutive elements of the flattened tensor; the last
+ *      block may be partial;
+ *  R7  the reduce is a plain sum (no division by the shard count) taken in
+ *      shard index order and starting from +0.0f;
+ *  R8  the FP8 accumulate adds in fp32: v = fl(fl(D8(c) * s) + g);
+ *  R9  a block whose scale is zero (all-zero block, or a scale that
+ *      underflows to zero) gets all-zero code bits.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+/* Element types and code formats. The numbering is an interface convention
+ * that the tests pass through; it is spelled out again here on purpose. */
+#define ORC_F32 0
+#define ORC_F16 1
+#define ORC_BF16 2
+
+#define ORC_INT2 2
+#define ORC_INT4 4
+#define ORC_INT6 6
+#define ORC_INT8 8
+#define ORC_E4M3 0x48
+
+#define ORC_OK 0
+#define ORC_BAD (-1)
+
+/* ------------------------------------------------------------------------ */
+/* Format helpers                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* Bits per code, or 0 for an unknown format. */
+static int code_bits(int fmt)
+{
+    switch (fmt) {
+    case ORC_INT2: return 2;
+    case ORC_INT4: return 4;
+    case ORC_INT6: return 6;
+    case ORC_INT8: return 8;
+    case ORC_E4M3: return 8;
+    default: return 0;
+    }
+}
+
+/* Largest integer code magnitude, 2^(b-1) - 1 (reading R2). */
+static int int_qmax(int fmt) { return (1 << (code_bits(fmt) - 1)) - 1; }
+
+static int valid_block(int64_t G)
+{
+    return G == 32 || G == 64 || G == 128 || G == 256 || G == 512 || G == 1024;
+}
+
+static int elem_size(int dtype)
+{
+    return dtype == ORC_F32 ? 4 : (dtype == ORC_F16 || dtype == ORC_BF16) ? 2 : 0;
+}
+
+/* Bytes of the packed code stream: ceil(n*b/32) 32-bit words (reading R5). */
+int64_t orc_codes_bytes(int fmt, int64_t n)
+{
+    int b = code_bits(fmt);
+    if (b == 0 || n < 0) return -1;
+    return ((n * b + 31) / 32) * 4;
+}
+
+/* Number of G-element blocks, ceil(n/G) (reading R6). */
+int64_t orc_num_blocks(int64_t n, int64_t G)
+{
+    if (n < 0 || !valid_block(G)) return -1;
+    return (n + G - 1) / G;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Binary floating-point formats, written from their definitions            */
+/* (IEEE 754 binary16 and binary32; bfloat16 = upper half of binary32;      */
+/* OCP 8-bit floating point E4M3: bias 7, no infinities, S.1111.111 = NaN,  */
+/* largest finite 448).                                                      */
+/* ------------------------------------------------------------------------ */
+
+/* Round a finite magnitude a >= 0 (a double holding a binary32 value) to the
+ * nearest value of a binary format with p significand bits (hidden bit
+ * included) and smallest normal exponent emin, ties to even. Values below
+ * 2^emin are rounded to multiples of 2^(emin-p+1) (gradual underflow). No
+ * overflow handling: the caller decides what happens above its largest value. */
+static double round_to_format(double a, int p, int emin)
+{
+    int k;
+    double quantum, t, r;
+    if (a == 0.0) return 0.0;
+    (void)frexp(a, &k);           /* a = f * 2^k with f in [0.5, 1) */
+    if (k - 1 < emin) k = emin + 1;
+    quantum = ldexp(1.0, (k - 1) - (p - 1));
+    t = a / quantum;              /* exact: division by a power of two */
+    r = nearbyint(t);             /* default mode: nearest, ties to even */
+    return r * quantum;           /* exact */
+}
+
+/* Exponent e with 2^e <= a < 2^(e+1), for a > 0. */
+static int exponent_of(double a)
+{
+    int k;
+    (void)frexp(a, &k);
+    return k - 1;
+}
+
+static float bits_to_f32(uint32_t u)
+{
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+static uint32_t f32_to_bits(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return u;
+}
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+float orc_f16_decode(uint32_t h)
+{
+    int sign = (h >> 15) & 1, ex = (h >> 10) & 31, fr = h & 1023;
+    double v;
+    if (ex == 0) v = ldexp((double)fr, -24);
+    else if (ex == 31) v = fr ? NAN : INFINITY;
+    else v = ldexp(1024.0 + fr, ex - 25);
+    return (float)(sign ? -v : v);
+}
+
+uint32_t orc_f16_encode(float x)
+{
+    uint32_t sign = signbit(x) ? 0x8000u : 0u;
+    double a = fabs((double)x), r;
+    int e;
+    if (isnan(x)) return 0x7E00u;
+    if (isinf(x)) return sign | 0x7C00u;
+    r = round_to_format(a, 11, -14);
+    if (r > 65504.0) return sign | 0x7C00u;          /* overflow to infinity */
+    if (r == 0.0) return sign;
+    if (r < ldexp(1.0, -14)) return sign | (uint32_t)(r / ldexp(1.0, -24));
+    e = exponent_of(r);
+    return sign | (uint32_t)(e + 15) << 10 | (uint32_t)((r / ldexp(1.0, e) - 1.0) * 1024.0);
+}
+
+/* bfloat16 is the upper 16 bits of a binary32 (8 significand bits). */
+float orc_bf16_decode(uint32_t h) { return bits_to_f32((h & 0xFFFFu) << 16); }
+
+uint32_t orc_bf16_encode(float x)
+{
+    uint32_t sign = signbit(x) ? 0x8000u : 0u;
+    double a = fabs((double)x), r;
+    if (isnan(x)) return 0x7FC0u;
+    if (isinf(x)) return sign | 0x7F80u;
+    r = round_to_format(a, 8, -126);
+    if (r > ldexp(255.0, 120)) return sign | 0x7F80u; /* above (2-2^-7)*2^127 */
+    /* r is a bfloat16 value, so it is exact in binary32; keep the top half. */
+    return sign | (f32_to_bits((float)r) >> 16);
+}
+
+/* E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits. */
+float orc_e4m3_decode(uint32_t c)
+{
+    int sign = (c >> 7) & 1, ex = (c >> 3) & 15, fr = c & 7;
+    double v;
+    if (ex == 15 && fr == 7) return NAN;
+    if (ex == 0) v = ldexp((double)fr, -9);
+    else v = ldexp(8.0 + fr, ex - 10);
+    return (float)(sign ? -v : v);
+}
+
+/* Round to nearest E4M3, ties to even, saturating to +-448 ("satfinite"). */
+uint32_t orc_e4m3_encode(float x)
+{
+    uint32_t sign = signbit(x) ? 0x80u : 0u;
+    double a = fabs((double)x), r;
+    int e;
+    if (isnan(x)) return 0x7Fu;
+    r = isinf(x) ? 448.0 : round_to_format(a, 4, -6);
+    if (r > 448.0) r = 448.0;
+    if (r == 0.0) return sign;
+    if (r < ldexp(1.0, -6)) return sign | (uint32_t)(r / ldexp(1.0, -9));
+    e = exponent_of(r);
+    return sign | (uint32_t)(e + 7) << 3 | (uint32_t)((r / ldexp(1.0, e) - 1.0) * 8.0);
+}
+
+/* Element i of a source buffer, widened exactly to binary32. */
+static float load_elem(const void *p, int dtype, int64_t i)
+{
+    if (dtype == ORC_F32) return ((const float *)p)[i];
+    if (dtype == ORC_F16) return orc_f16_decode(((const uint16_t *)p)[i]);
+    return orc_bf16_decode(((const uint16_t *)p)[i]);
+}
+
+/* Store a binary32 value as element i of a destination buffer (one RNE
+ * rounding for the 16-bit types). */
+static void store_elem(void *p, int dtype, int64_t i, float v)
+{
+    if (dtype == ORC_F32) ((float *)p)[i] = v;
+    else if (dtype == ORC_F16) ((uint16_t *)p)[i] = (uint16_t)orc_f16_encode(v);
+    else ((uint16_t *)p)[i] = (uint16_t)orc_bf16_encode(v);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Bit stream (reading R5)                                                  */
+/* ------------------------------------------------------------------------ */
+
+static void put_bits(uint8_t *stream, int64_t pos, int nbits, uint32_t value)
+{
+    int k;
+    for (k = 0; k < nbits; ++k)
+        if ((value >> k) & 1u) stream[(pos + k) >> 3] |= (uint8_t)(1u << ((pos + k) & 7));
+}
+
+static uint32_t get_bits(const uint8_t *stream, int64_t pos, int nbits)
+{
+    uint32_t v = 0;
+    int k;
+    for (k = 0; k < nbits; ++k)
+        v |= (uint32_t)((stream[(pos + k) >> 3] >> ((pos + k) & 7)) & 1u) << k;
+    return v;
+}
+
+/* ------------------------------------------------------------------------ */
+/* One block: absmax, scale, codes                                          */
+/* ------------------------------------------------------------------------ */
+
+/* Quantize the values v[0..len) of one block into the stream at element
+ * offset first; returns the block's scale. [ZeRO++] qwZ section; [Aquavit]
+ * Eq. 6; [AGoQ] 2.B for the E4M3 case. */
+static float quantize_block(const float *v, int64_t len, int fmt, uint8_t *codes, int64_t first)
+{
+    int b = code_bits(fmt);
+    float m = 0.0f, s;
+    int64_t i;
+
+    /* absmax over the block (exact, order free) */
+    for (i = 0; i < len; ++i)
+        if (fabsf(v[i]) > m) m = fabsf(v[i]);
+
+    /* scale: one IEEE binary32 division (R2, R3) */
+    if (fmt == ORC_E4M3) s = m / 448.0f;
+    else s = m / (float)int_qmax(fmt);
+
+    for (i = 0; i < len; ++i) {
+        uint32_t c;
+        if (s == 0.0f) {
+            c = 0; /* R9 */
+        } else if (fmt == ORC_E4M3) {
+            float t = v[i] / s;
+            c = orc_e4m3_encode(t);
+        } else {
+            int qmax = int_qmax(fmt);
+            float t = v[i] / s;      /* IEEE division, R4 */
+            float q = nearbyintf(t); /* ties to even, R3 */
+            if (q > (float)qmax) q = (float)qmax;
+            if (q < (float)-qmax) q = (float)-qmax;
+            c = (uint32_t)(int32_t)q & ((1u << b) - 1u); /* two's complement */
+        }
+        put_bits(codes, (first + i) * b, b, c);
+    }
+    return s;
+}
+
+/* Value of code element i: the integer code, or the E4M3 value, times s. */
+static float dequant_elem(const uint8_t *codes, float s, int fmt, int64_t i)
+{
+    int b = code_bits(fmt);
+    uint32_t c = get_bits(codes, i * b, b);
+    if (fmt == ORC_E4M3) return orc_e4m3_decode(c) * s;
+    {
+        int32_t q = (int32_t)c;
+        if (c & (1u << (b - 1))) q -= (int32_t)(1u << b); /* sign extend */
+        return (float)q * s;                                /* one binary32 multiply */
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Public oracle entry points                                               */
+/* ------------------------------------------------------------------------ */
+
+/* One block of widened values (G <= 1024). */
+static float scratch[1024];
+
+/* Quantize n elements of src (dtype) into packed codes and one scale per
+ * block. codes must hold orc_codes_bytes(fmt, n) bytes, scales
+ * orc_num_blocks(n, G) floats. */
+int orc_quantize(const void *src, int dtype, int64_t n, int fmt, int64_t G, uint8_t *codes,
+                 float *scales)
+{
+    int64_t k, i, nb;
+    if (!code_bits(fmt) || !valid_block(G) || !elem_size(dtype) || n < 0) return ORC_BAD;
+    memset(codes, 0, (size_t)orc_codes_bytes(fmt, n));
+    nb = orc_num_blocks(n, G);
+    for (k = 0; k < nb; ++k) {
+        int64_t lo = k * G, len = (n - lo < G) ? n - lo : G;
+        for (i = 0; i < len; ++i) scratch[i] = load_elem(src, dtype, lo + i);
+        scales[k] = quantize_block(scratch, len, fmt, codes, lo);
+    }
+    return ORC_OK;
+}
+
+/* Dequantize: y = fl32(q * s), then one RNE rounding to dst_dtype. */
+int orc_dequantize(const uint8_t *codes, const float *scales, int64_t n, int fmt, int64_t G,
+                   void *dst, int dst_dtype)
+{
+    int64_t i;
+    if (!code_bits(fmt) || !valid_block(G) || !elem_size(dst_dtype) || n < 0) return ORC_BAD;
+    for (i = 0; i < n; ++i) store_elem(dst, dst_dtype, i, dequant_elem(codes, scales[i / G], fmt, i));
+    return ORC_OK;
+}
+
+/* Quantized reduce ([ZeRO++] qgZ; [AGoQ] Local Reduce): for every element,
+ * acc = +0.0f, then acc = fl(acc + D(shard r)) for r = 0..nshards-1 in
+ * order; optionally store acc; then quantize acc with (fmt_out, G_out). */
+int orc_reduce(const uint8_t *const *codes, const float *const *scales, int nshards, int64_t n,
+               int fmt_in, int64_t G_in, uint8_t *out_codes, float *out_scales, int fmt_out,
+               int64_t G_out, float *sum_out)
+{
+    int64_t k, i, nb;
+    int r;
+    if (!code_bits(fmt_in) || !code_bits(fmt_out) || !valid_block(G_in) || !valid_block(G_out) ||
+        nshards < 1 || n < 0)
+        return ORC_BAD;
+    memset(out_codes, 0, (size_t)orc_codes_bytes(fmt_out, n));
+    nb = orc_num_blocks(n, G_out);
+    for (k = 0; k < nb; ++k) {
+        int64_t lo = k * G_out, len = (n - lo < G_out) ? n - lo : G_out;
+        for (i = 0; i < len; ++i) {
+            float acc = 0.0f;
+            for (r = 0; r < nshards; ++r) {
+                float d = dequant_elem(codes[r], scales[r][(lo + i) / G_in], fmt_in, lo + i);
+                acc = acc + d; /* one binary32 addition per shard, in shard order */
+            }
+            scratch[i] = acc;
+            if (sum_out) sum_out[lo + i] = acc;
+        }
+        out_scales[k] = quantize_block(scratch, len, fmt_out, out_codes, lo);
+    }
+    return ORC_OK;
+}
+
+/* FP8 gradient accumulation in place ([AGoQ] Local Accumulation, reading R8):
+ * v = fl(fl(D8(c) * s) + g), then E4M3 requantization of v with block G. */
+int orc_fp8_accumulate(uint8_t *codes, float *scales, const void *grad, int grad_dtype, int64_t n,
+                       int64_t G)
+{
+    int64_t k, i, nb;
+    if (!valid_block(G) || !elem_size(grad_dtype) || n < 0) return ORC_BAD;
+    nb = orc_num_blocks(n, G);
+    for (k = 0; k < nb; ++k) {
+        int64_t lo = k * G, len = (n - lo < G) ? n - lo : G;
+        for (i = 0; i < len; ++i) {
+            float d = orc_e4m3_decode(codes[lo + i]) * scales[k];
+            scratch[i] = d + load_elem(grad, grad_dtype, lo + i);
+        }
+        /* the block's old code bytes are replaced by the new ones */
+        for (i = 0; i < len; ++i) codes[lo + i] = 0;
+        scales[k] = quantize_block(scratch, len, ORC_E4M3, codes, lo);
+    }
+    return ORC_OK;
+}
+
+/* Array forms of the codecs (kind = ORC_F16, ORC_BF16 or ORC_E4M3), so that
+ * the tests can check every bit pattern without one foreign call per value. */
+int orc_encode_n(int kind, const float *x, int64_t n, uint32_t *out)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i) {
+        if (kind == ORC_F16) out[i] = orc_f16_encode(x[i]);
+        else if (kind == ORC_BF16) out[i] = orc_bf16_encode(x[i]);
+        else if (kind == ORC_E4M3) out[i] = orc_e4m3_encode(x[i]);
+        else return ORC_BAD;
+    }
+    return ORC_OK;
+}
+
+int orc_decode_n(int kind, const uint32_t *c, int64_t n, float *out)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i) {
+        if (kind == ORC_F16) out[i] = orc_f16_decode(c[i]);
+        else if (kind == ORC_BF16) out[i] = orc_bf16_decode(c[i]);
+        else if (kind == ORC_E4M3) out[i] = orc_e4m3_decode(c[i]);
+        else return ORC_BAD;
+    }
+    return ORC_OK;
+}

@@ -1,0 +1,607 @@
+"""Pins for the oracle: checks against what the pages, the format specifications
+and the mathematics fix, independent of the oracle's own code.
+
+Each ``pin_*`` takes a loaded oracle library (so that the mutation tests can
+run the same checks against deliberately broken builds) and raises
+AssertionError on a mismatch. Sizes are kept small so that the whole set runs
+in seconds; the exhaustive variants live in the test modules.
+
+Independent routes used here (none of them re-runs the oracle's formula):
+  * values printed on the pages (tests/golden/*.json, each with its source);
+  * the OCP FP8 and IEEE 754 format definitions, through torch's float8 and
+    bfloat16 conversions and numpy's float16 conversion (library routines);
+  * exact rational arithmetic (fractions.Fraction) for divisions and roundings;
+  * correctly rounded binary32 quotients obtained as binary64 quotients rounded
+    to binary32 (double rounding is innocuous for division when the wide
+    format has at least 2p+2 bits: S. Figueroa, "When is double rounding
+    innocuous?", SIGNUM Newsletter 30(3), 1995);
+  * closed forms (power-of-two scales make every product and partial sum
+    exact, so fp32 results must equal integer arithmetic);
+  * invariants (block independence, idempotence, error bounds).
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+INT_FORMATS = (O.INT2, O.INT4, O.INT6, O.INT8)
+ALL_FORMATS = INT_FORMATS + (O.E4M3,)
+BLOCKS = (32, 64, 128, 256, 512, 1024)
+
+
+def golden(name: str) -> dict:
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def qmax(fmt: int) -> int:
+    return (1 << (O.BITS[fmt] - 1)) - 1
+
+
+# ---------------------------------------------------------------------------
+# exact helpers (independent of the oracle)
+# ---------------------------------------------------------------------------
+
+def rn32(v: Fraction) -> Fraction:
+    """Nearest binary32 value to the rational v (ties to even), by exact arithmetic."""
+    if v == 0:
+        return Fraction(0)
+    sign = -1 if v < 0 else 1
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    e = max(e, -126)
+    quantum = Fraction(2) ** (e - 23)
+    r = round(a / quantum)  # Fraction rounds half to even
+    return sign * r * quantum
+
+
+def div32(x: np.ndarray, s) -> np.ndarray:
+    """Correctly rounded binary32 quotient x/s via a binary64 quotient (Figueroa)."""
+    return (np.asarray(x, dtype=np.float64) / np.float64(s)).astype(np.float32)
+
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32)
+
+
+def torch_bf16_bits(x32: np.ndarray) -> np.ndarray:
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(x32, np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+
+
+def torch_e4m3_codes(x32: np.ndarray) -> np.ndarray:
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(x32, np.float32)).to(torch.float8_e4m3fn) \
+        .view(torch.uint8).numpy()
+
+
+def unpack_codes(codes: np.ndarray, n: int, bits: int) -> np.ndarray:
+    """Signed integer codes from the LSB-first stream, read with numpy's bit unpacking."""
+    stream = np.unpackbits(codes, bitorder="little")[: n * bits].reshape(n, bits).astype(np.int64)
+    vals = (stream << np.arange(bits)).sum(axis=1)
+    return np.where(vals >= (1 << (bits - 1)), vals - (1 << bits), vals)
+
+
+def rng(seed: int) -> np.random.Generator:
+    return np.random.default_rng(seed)
+
+
+# ---------------------------------------------------------------------------
+# sizes and payloads printed on the pages
+# ---------------------------------------------------------------------------
+
+def pin_bpw_endpoints(lib):
+    """Aquavit Table 1 endpoints: 2-bit/G=1024 -> 2.03 bpw, 6-bit/G=32 -> 7.00 bpw."""
+    g = golden("granularity_modulation_bpw.json")
+    fmt_of = {2: O.INT2, 4: O.INT4, 6: O.INT6, 8: O.INT8}
+    x = rng(1).standard_normal(8192).astype(np.float32)
+    for e in g["printed_endpoints"]:
+        codes, scales = O.quantize(x, fmt_of[e["bits"]], e["G"], lib=lib)
+        bpw = (codes.nbytes + scales.nbytes) * 8 / x.size
+        assert f"{bpw:.2f}" == e["bpw_printed"], (e, bpw)
+
+
+def pin_bpw_formula(lib):
+    """Eq. 6 of the Aquavit page, bpw = b + 32/G, for every (b, G) of the sweep."""
+    g = golden("granularity_modulation_bpw.json")
+    fmt_of = {2: O.INT2, 4: O.INT4, 6: O.INT6, 8: O.INT8}
+    n = 4096
+    x = rng(2).standard_normal(n).astype(np.float32)
+    for b in g["bits"]:
+        for G in g["block_sizes"]:
+            codes, scales = O.quantize(x, fmt_of[b], G, lib=lib)
+            assert Fraction((codes.nbytes + scales.nbytes) * 8, n) == b + Fraction(32, G), (b, G)
+
+
+def pin_zeropp_payload(lib):
+    """ZeRO++: 3M -> 0.75M = 0.5M (int8 weights) + 0 (hpZ) + 0.25M (int4 gradients)."""
+    g = golden("zeropp_payload.json")
+    n = 1 << 14
+    w = rng(3).standard_normal(n).astype(np.float16)
+    fp16_bytes = w.nbytes
+    c8, _ = O.quantize(w, O.INT8, 256, lib=lib)
+    c4, _ = O.quantize(w.astype(np.float32), O.INT4, 128, lib=lib)
+    parts = g["parts"]
+    assert Fraction(c8.nbytes, fp16_bytes) == Fraction(parts["forward_allgather_int8_weights"])
+    assert Fraction(c4.nbytes, fp16_bytes) == Fraction(parts["gradient_reduce_int4"])
+    total = Fraction(c8.nbytes + 0 + c4.nbytes, fp16_bytes)
+    assert total == Fraction(g["zeropp_total_in_M"]) and g["baseline_collectives_in_M"] == 3.0
+
+
+def pin_bit_layout(lib):
+    """Hand-derived packed bytes for each code width (scale exactly 1)."""
+    fmt_of = {2: O.INT2, 4: O.INT4, 6: O.INT6, 8: O.INT8}
+    for case in golden("bit_layout.json")["cases"]:
+        x = np.array(case["values"], dtype=np.float32)
+        codes, scales = O.quantize(x, fmt_of[case["bits"]], 32, lib=lib)
+        assert scales[0] == 1.0, case
+        assert codes.tobytes().hex() == case["bytes"], (case, codes.tobytes().hex())
+
+
+# ---------------------------------------------------------------------------
+# number formats
+# ---------------------------------------------------------------------------
+
+def pin_e4m3_points(lib):
+    g = golden("e4m3_points.json")
+    for e in g["encode"]:
+        got = O.encode_array("e4m3", np.array([e["x"]], np.float32), lib=lib)[0]
+        assert got == int(e["code"], 16), (e, hex(got))
+    for e in g["decode"]:
+        got = O.decode_array("e4m3", np.array([int(e["code"], 16)]), lib=lib)[0]
+        if e["x"] == "nan":
+            assert math.isnan(got), e
+        else:
+            assert got == e["x"], (e, got)
+
+
+def pin_e4m3_vs_library(lib, n_random=200_000):
+    """All 256 decodes, and encodes of random values, midpoints and their neighbours."""
+    import torch
+
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    got = O.decode_array("e4m3", codes.astype(np.uint32), lib=lib)
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok].view(np.uint32), got[ok].view(np.uint32))
+    # midpoints between consecutive finite magnitudes, and one binary32 ulp either side
+    mags = np.unique(np.abs(ref[ok]).astype(np.float64))
+    mids = ((mags[1:] + mags[:-1]) / 2).astype(np.float32)
+    around = np.concatenate([mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1e9)),
+                             mags.astype(np.float32)])
+    r = rng(4)
+    rand = (r.uniform(-1, 1, n_random) * 2.0 ** r.integers(-14, 9, n_random)).astype(np.float32)
+    x = np.concatenate([around, -around, rand])
+    x = x[np.abs(x) < 464]  # the library maps values at and above 464 to NaN, not to 448
+    assert np.array_equal(O.encode_array("e4m3", x, lib=lib), torch_e4m3_codes(x).astype(np.uint32))
+
+
+def pin_f16_vs_library(lib, n_random=200_000):
+    allbits = np.arange(65536, dtype=np.uint32)
+    ref = allbits.astype(np.uint16).view(np.float16).astype(np.float32)
+    got = O.decode_array("f16", allbits, lib=lib)
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(ref[~nan].view(np.uint32), got[~nan].view(np.uint32))
+    r = rng(5)
+    finite = ref[~nan & np.isfinite(ref)].astype(np.float64)
+    mags = np.unique(np.abs(finite))
+    mids = ((mags[1:] + mags[:-1]) / 2).astype(np.float32)
+    rand = (r.uniform(-1, 1, n_random) * 2.0 ** r.integers(-30, 17, n_random)).astype(np.float32)
+    x = np.concatenate([mids, -mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1e9)), rand])
+    assert np.array_equal(O.encode_array("f16", x, lib=lib), x.astype(np.float16).view(np.uint16).astype(np.uint32))
+
+
+def pin_bf16_vs_library(lib, n_random=200_000):
+    import torch
+
+    allbits = np.arange(65536, dtype=np.uint32)
+    ref = torch.from_numpy(allbits.astype(np.uint16).view(np.int16)).view(torch.bfloat16).float().numpy()
+    got = O.decode_array("bf16", allbits, lib=lib)
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(ref[~nan].view(np.uint32), got[~nan].view(np.uint32))
+    r = rng(6)
+    bits = r.integers(0, 1 << 32, n_random, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x) & (np.abs(x) < 3.3e38)]
+    # exact ties: the low 16 bits equal to 0x8000
+    ties = ((bits & 0xFFFF0000) | 0x8000).view(np.float32)
+    ties = ties[np.isfinite(ties) & (np.abs(ties) < 3.3e38)]
+    x = np.concatenate([x, ties])
+    assert np.array_equal(O.encode_array("bf16", x, lib=lib), torch_bf16_bits(x).astype(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# quantize: scale, rounding, clamp, packing
+# ---------------------------------------------------------------------------
+
+def expected_int_codes(x32: np.ndarray, fmt: int, G: int):
+    """Codes and scales of the definition, by an independent route (Figueroa
+    quotients, numpy rint, explicit clamp); blocks of G along x32."""
+    n = x32.size
+    nb = (n + G - 1) // G
+    qm = qmax(fmt)
+    scales = np.zeros(nb, np.float32)
+    q = np.zeros(n, np.int64)
+    for k in range(nb):
+        blk = x32[k * G:(k + 1) * G]
+        m = np.float32(np.max(np.abs(blk))) if blk.size else np.float32(0)
+        s = div32(np.array([m]), qm)[0]
+        scales[k] = s
+        if s == 0:
+            continue
+        t = div32(blk, s)
+        q[k * G:(k + 1) * G] = np.clip(np.rint(t).astype(np.int64), -qm, qm)
+    return q, scales
+
+
+def pin_rounding_exhaustive_16bit(lib, fmt=O.INT4, src="bf16", absmax=1.2265625):
+    """Every finite 16-bit value x with |x| <= M placed in blocks led by M:
+    codes and scales equal the definition computed by an independent route."""
+    G = 32
+    allbits = np.arange(65536, dtype=np.uint32)
+    M = np.float32(absmax)  # exact in bf16 and fp16
+    if src == "bf16":
+        vals = bf16_to_f32(allbits)
+    else:
+        vals = allbits.astype(np.uint16).view(np.float16).astype(np.float32)
+    keep = np.isfinite(vals) & (np.abs(vals) <= M)
+    test_bits = allbits[keep]
+    nblk = (test_bits.size + G - 2) // (G - 1)
+    pad = nblk * (G - 1) - test_bits.size
+    test_bits = np.concatenate([test_bits, np.zeros(pad, np.uint32)])
+    lead_bits = (M.view(np.uint32) >> 16) if src == "bf16" else np.float16(M).view(np.uint16)
+    blocks = np.concatenate([np.full((nblk, 1), lead_bits, np.uint32), test_bits.reshape(nblk, G - 1)], axis=1)
+    bits16 = blocks.reshape(-1).astype(np.uint16)
+    x32 = bf16_to_f32(bits16) if src == "bf16" else bits16.view(np.float16).astype(np.float32)
+    dtype = O.BF16 if src == "bf16" else O.F16
+    codes, scales = O.quantize(bits16 if src == "bf16" else bits16.view(np.float16), fmt, G, dtype=dtype, lib=lib)
+    q_ref, s_ref = expected_int_codes(x32, fmt, G)
+    assert np.array_equal(scales.view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(unpack_codes(codes, x32.size, O.BITS[fmt]), q_ref)
+
+
+def pin_rounding_fractions(lib, n=600):
+    """Exact rational check: s = RN32(m/qmax), code = round-half-even(RN32(x/s)), clamped."""
+    r = rng(7)
+    for fmt in INT_FORMATS:
+        x = (r.standard_normal(n) * 0.05).astype(np.float32)
+        codes, scales = O.quantize(x, fmt, 32, lib=lib)
+        q = unpack_codes(codes, n, O.BITS[fmt])
+        qm = qmax(fmt)
+        for k in range(n // 32 + (n % 32 > 0)):
+            blk = x[k * 32:(k + 1) * 32]
+            m = max(Fraction(float(abs(v))) for v in blk)
+            s = rn32(m / qm)
+            assert Fraction(float(scales[k])) == s
+            for i, v in enumerate(blk):
+                want = max(-qm, min(qm, round(rn32(Fraction(float(v)) / s))))
+                assert q[k * 32 + i] == want, (fmt, k, i, float(v))
+
+
+def pin_exact_multiples_and_ties(lib):
+    """Power-of-two scale: x = k*s gives code k; x = (k+1/2)*s goes to the even neighbour."""
+    for fmt in INT_FORMATS:
+        qm = qmax(fmt)
+        s = 2.0 ** -7
+        ks = np.arange(-qm, qm + 1)
+        x = np.concatenate([[qm * s], ks * s]).astype(np.float32)
+        codes, scales = O.quantize(x, fmt, 32 if x.size <= 32 else 256, lib=lib)
+        assert scales[0] == np.float32(s)
+        assert np.array_equal(unpack_codes(codes, x.size, O.BITS[fmt])[1:], ks)
+        if qm >= 3:
+            halves = np.arange(-qm + 1, qm - 1) + 0.5  # k + 1/2 strictly inside the range
+            x = np.concatenate([[qm * s], halves * s]).astype(np.float32)
+            codes, _ = O.quantize(x, fmt, 256, lib=lib)
+            want = np.round(halves).astype(np.int64)  # numpy rounds halves to even
+            assert np.array_equal(unpack_codes(codes, x.size, O.BITS[fmt])[1:], want), fmt
+
+
+def pin_zero_and_tiny_blocks(lib):
+    """All-zero block -> scale 0 and zero codes; subnormal scales still give codes in range."""
+    for fmt in ALL_FORMATS:
+        x = np.zeros(64, np.float32)
+        x[32:] = np.float32(1.0)
+        codes, scales = O.quantize(x, fmt, 32, lib=lib)
+        assert scales[0] == 0.0 and not np.any(codes[: O.BITS[fmt] * 32 // 8])
+    # bf16 subnormal inputs: the scale is subnormal, the code must still be the definition's
+    tiny_bits = np.array([0x0001, 0x0003, 0x8002, 0x0000, 0x0005] * 7, np.uint16)[:32]
+    x32 = bf16_to_f32(tiny_bits)
+    for fmt in INT_FORMATS:
+        codes, scales = O.quantize(tiny_bits, fmt, 32, dtype=O.BF16, lib=lib)
+        q_ref, s_ref = expected_int_codes(x32, fmt, 32)
+        assert np.array_equal(scales.view(np.uint32), s_ref.view(np.uint32))
+        assert np.array_equal(unpack_codes(codes, 32, O.BITS[fmt]), q_ref), fmt
+        assert np.all(np.abs(q_ref) <= qmax(fmt))
+    # fp32 subnormals: m = 300 * 2^-149 and qmax = 127 give s = 2 * 2^-149, so
+    # m / s = 150 and the clamp to 127 decides the code
+    ulp0 = np.float32(2.0 ** -149)
+    x = (np.array([300, -300, 299, 255, 254, -256, 3, 0] * 4, np.float64) * 2.0 ** -149).astype(np.float32)
+    q_ref, s_ref = expected_int_codes(x, O.INT8, 32)
+    assert s_ref[0] == 2 * ulp0 and np.rint(div32(x, s_ref[0])).max() > 127
+    codes, scales = O.quantize(x, O.INT8, 32, lib=lib)
+    assert scales[0] == s_ref[0]
+    assert np.array_equal(unpack_codes(codes, x.size, 8), q_ref)
+
+
+def pin_e4m3_quantize(lib, n=4096):
+    """E4M3 codes: s = RN32(m/448), code = E4M3_RNE_satfinite(RN32(x/s)) via the library encoder."""
+    r = rng(8)
+    x = (r.standard_normal(n) * 1e-3).astype(np.float32)
+    x[::97] *= 40
+    for G in (32, 128, 1024):
+        codes, scales = O.quantize(x, O.E4M3, G, lib=lib)
+        for k in range(n // G):
+            blk = x[k * G:(k + 1) * G]
+            s = div32(np.array([np.max(np.abs(blk))]), 448)[0]
+            assert scales[k] == s
+            want = torch_e4m3_codes(div32(blk, s))
+            assert np.array_equal(codes[k * G:(k + 1) * G], want), (G, k)
+
+
+def pin_block_independence(lib):
+    """Quantizing a concatenation of whole blocks equals concatenating the pieces;
+    a partial last block uses only its own elements."""
+    r = rng(9)
+    for fmt in ALL_FORMATS:
+        for G in (32, 256):
+            a = (r.standard_normal(3 * G) * 0.02).astype(np.float32)
+            b = (r.standard_normal(G // 2 + 3) * 0.5).astype(np.float32)
+            ca, sa = O.quantize(a, fmt, G, lib=lib)
+            cb, sb = O.quantize(b, fmt, G, lib=lib)
+            cab, sab = O.quantize(np.concatenate([a, b]), fmt, G, lib=lib)
+            assert np.array_equal(sab, np.concatenate([sa, sb]))
+            bits = O.BITS[fmt]
+            na = a.size * bits // 8
+            assert np.array_equal(cab[:na], ca[:na])
+            nb = (b.size * bits + 7) // 8
+            assert np.array_equal(cab[na:na + nb], cb[:nb])
+            assert not np.any(cab[na + nb:])  # zero padding
+
+
+def pin_roundtrip_bound(lib):
+    """|x - D(Q(x))| <= s * (1/2 + 2^-22 * qmax) for integer codes with fp32 output;
+    E4M3: |x - D| <= 2^-4 |x| + 2^-10 s + 2^-23 |x| (half an E4M3 ulp, plus rounding)."""
+    r = rng(10)
+    n = 8192
+    x = np.concatenate([(r.standard_normal(n // 2) * 0.02), r.laplace(0, 1e-4, n // 2)]).astype(np.float32)
+    x[::331] *= 50
+    for fmt in ALL_FORMATS:
+        for G in (32, 1024):
+            codes, scales = O.quantize(x, fmt, G, lib=lib)
+            y = O.dequantize(codes, scales, n, fmt, G, O.F32, lib=lib)
+            s = np.repeat(scales, G)[:n].astype(np.float64)
+            err = np.abs(x.astype(np.float64) - y)
+            if fmt == O.E4M3:
+                bound = 2.0 ** -4 * np.abs(x) + 2.0 ** -10 * s + 2.0 ** -22 * np.abs(x)
+            else:
+                bound = s * (0.5 + 2.0 ** -22 * qmax(fmt))
+            assert np.all(err <= bound), (fmt, G, float(np.max(err / np.maximum(bound, 1e-30))))
+
+
+def pin_idempotence(lib):
+    """Q(D(Q(x))) reproduces the codes; scales move by at most one binary32 ulp."""
+    r = rng(11)
+    n = 4096
+    x = (r.standard_normal(n) * 0.02).astype(np.float32)
+    for fmt in ALL_FORMATS:
+        for G in (32, 128):
+            c1, s1 = O.quantize(x, fmt, G, lib=lib)
+            y = O.dequantize(c1, s1, n, fmt, G, O.F32, lib=lib)
+            c2, s2 = O.quantize(y, fmt, G, lib=lib)
+            assert np.array_equal(c1, c2), (fmt, G)
+            ulps = np.abs(s1.view(np.int32).astype(np.int64) - s2.view(np.int32).astype(np.int64))
+            assert np.all(ulps <= 1), (fmt, G)
+
+
+def pin_dequant_values(lib):
+    """Dequantized fp32 = code value * scale as a single binary32 product, checked
+    with exact rationals; bf16/f16 outputs are one nearest-even rounding of it
+    (torch and numpy conversions)."""
+    r = rng(12)
+    n = 2048
+    x = (r.standard_normal(n) * 0.03).astype(np.float32)
+    for fmt in ALL_FORMATS:
+        G = 64
+        codes, scales = O.quantize(x, fmt, G, lib=lib)
+        y32 = O.dequantize(codes, scales, n, fmt, G, O.F32, lib=lib)
+        if fmt == O.E4M3:
+            vals = O.decode_array("e4m3", codes[:n].astype(np.uint32), lib=lib)
+            import torch
+            vals_lib = torch.from_numpy(codes[:n].copy()).view(torch.float8_e4m3fn).float().numpy()
+            assert np.array_equal(vals, vals_lib)
+        else:
+            vals = unpack_codes(codes, n, O.BITS[fmt]).astype(np.float32)
+        for i in range(0, n, 7):
+            want = rn32(Fraction(float(vals[i])) * Fraction(float(scales[i // G])))
+            assert Fraction(float(y32[i])) == want, (fmt, i)
+        ybf = O.dequantize(codes, scales, n, fmt, G, O.BF16, lib=lib)
+        assert np.array_equal(ybf, torch_bf16_bits(y32))
+        yh = O.dequantize(codes, scales, n, fmt, G, O.F16, lib=lib)
+        assert np.array_equal(yh, y32.astype(np.float16).view(np.uint16))
+
+
+# ---------------------------------------------------------------------------
+# reduce
+# ---------------------------------------------------------------------------
+
+def _shards(r, N, n, fmt, G, scale=1e-4):
+    out = []
+    for _ in range(N):
+        x = r.laplace(0, scale, n).astype(np.float32)
+        out.append(O.quantize(x, fmt, G))
+    return out
+
+
+def pin_reduce_single_shard(lib):
+    """N = 1: the reduce is dequantize (fp32) followed by quantize."""
+    r = rng(13)
+    for fin, Gin, fout, Gout in ((O.INT4, 128, O.INT4, 128), (O.INT4, 128, O.INT8, 256),
+                                 (O.E4M3, 128, O.E4M3, 128), (O.INT8, 64, O.INT2, 32)):
+        n = 2048 + 64
+        (c, s), = _shards(r, 1, n, fin, Gin)
+        oc, os_, sm = O.reduce([c], [s], n, fin, Gin, fout, Gout, want_sum=True, lib=lib)
+        y = O.dequantize(c, s, n, fin, Gin, O.F32, lib=lib)
+        assert np.array_equal(sm.view(np.uint32), y.view(np.uint32))
+        c2, s2 = O.quantize(y, fout, Gout, lib=lib)
+        assert np.array_equal(oc, c2) and np.array_equal(os_, s2)
+
+
+def pin_reduce_pow2_exact(lib):
+    """Power-of-two scales make every term and partial sum exact: the fp32 sum
+    equals the integer sum of codes times the scale."""
+    r = rng(14)
+    N, n, G = 8, 1024, 128
+    fmt = O.INT4
+    k = 12
+    codes, scales, qs = [], [], []
+    for _ in range(N):
+        q = r.integers(-7, 8, n)
+        q[::G] = 7  # absmax = 7 * 2^-k in every block, so s = 2^-k exactly
+        x = (q * 2.0 ** -k).astype(np.float32)
+        c, s = O.quantize(x, fmt, G, lib=lib)
+        assert np.all(s == np.float32(2.0 ** -k))
+        codes.append(c)
+        scales.append(s)
+        qs.append(q)
+    _, _, sm = O.reduce(codes, scales, n, fmt, G, O.INT8, 256, want_sum=True, lib=lib)
+    want = np.sum(qs, axis=0) * 2.0 ** -k
+    assert np.array_equal(sm.astype(np.float64), want)
+
+
+def pin_reduce_order(lib):
+    """Shard order is the summation order: 1 + 2^-24 + 2^-24 is 1 in fp32 when
+    summed left to right, but 1 + 2^-23 when summed right to left."""
+    n, G = 32, 32
+    vals = [1.0, 2.0 ** -24, 2.0 ** -24]
+    codes, scales = [], []
+    for v in vals:
+        x = np.full(n, np.float32(v))
+        c, s = O.quantize(x, O.INT2, G, lib=lib)  # qmax = 1, so s = v and codes = 1
+        codes.append(c)
+        scales.append(s)
+    _, _, sm = O.reduce(codes, scales, n, O.INT2, G, O.INT8, G, want_sum=True, lib=lib)
+    assert np.all(sm == np.float32(1.0))
+    _, _, sm_rev = O.reduce(codes[::-1], scales[::-1], n, O.INT2, G, O.INT8, G, want_sum=True, lib=lib)
+    assert np.all(sm_rev == np.float32(1.0 + 2.0 ** -23))
+
+
+def pin_reduce_plain_sum_and_bound(lib):
+    """The reduce is a sum, not a mean, and stays within the recursive-summation
+    bound (N-1) u sum|d_r| of the exact sum (Higham, Accuracy and Stability of
+    Numerical Algorithms, 2nd ed., section 4.2)."""
+    r = rng(15)
+    N, n = 8, 4096
+    sh = _shards(r, N, n, O.INT4, 128)
+    _, _, sm = O.reduce([c for c, _ in sh], [s for _, s in sh], n, O.INT4, 128, O.INT4, 128,
+                        want_sum=True, lib=lib)
+    terms = np.array([O.dequantize(c, s, n, O.INT4, 128, O.F32, lib=lib) for c, s in sh], np.float64)
+    exact = terms.sum(axis=0)
+    bound = (N - 1) * 2.0 ** -24 * np.abs(terms).sum(axis=0) * (1 + 1e-6)
+    assert np.all(np.abs(sm - exact) <= bound)
+    # two identical shards sum to exactly twice the value
+    c, s = sh[0]
+    _, _, two = O.reduce([c, c], [s, s], n, O.INT4, 128, O.INT4, 128, want_sum=True, lib=lib)
+    assert np.array_equal(two, 2 * terms[0].astype(np.float32))
+
+
+def pin_reduce_two_roundings(lib):
+    """Each term is rounded before it is added: with codes (-3, 3) and scales
+    (1, 1 + 2^-23) the definition gives fl(-3 + fl(3 (1 + 2^-23))) = 2^-21,
+    while a fused multiply-add would give 3 * 2^-23."""
+    n, G = 32, 32
+    c0 = np.zeros(n * 8 // 8, np.uint8)
+    c0[:] = np.uint8(0xFD)  # int8 code -3
+    c1 = np.full(n, 3, np.uint8)
+    s0 = np.array([1.0], np.float32)
+    s1 = np.array([1.0 + 2.0 ** -23], np.float32)
+    _, _, sm = O.reduce([c0, c1], [s0, s1], n, O.INT8, G, O.INT8, G, want_sum=True, lib=lib)
+    want = rn32(rn32(Fraction(-3)) + rn32(3 * Fraction(float(s1[0]))))
+    assert want == Fraction(2) ** -21
+    assert all(Fraction(float(v)) == want for v in sm)
+
+
+def pin_fp8_reduce_no_overflow(lib):
+    """AGoQ's precision-preserved reduce: eight FP8 shards at the E4M3 maximum sum
+    to 8 * 448 = 3584 with no saturation, because the result gets its own scale."""
+    n, G = 128, 128
+    x = np.full(n, np.float32(448.0))
+    c, s = O.quantize(x, O.E4M3, G, lib=lib)
+    assert s[0] == 1.0 and np.all(c == 0x7E)
+    oc, os_, sm = O.reduce([c] * 8, [s] * 8, n, O.E4M3, G, O.E4M3, G, want_sum=True, lib=lib)
+    assert np.all(sm == 3584.0) and os_[0] == 8.0 and np.all(oc == 0x7E)
+    y = O.dequantize(oc, os_, n, O.E4M3, G, O.F32, lib=lib)
+    assert np.all(y == 3584.0)
+
+
+# ---------------------------------------------------------------------------
+# FP8 accumulate
+# ---------------------------------------------------------------------------
+
+def pin_fp8_accumulate(lib):
+    """Zero main gradient: accumulate(g) == Q8(g). Zero gradient: codes unchanged.
+    Four steps stay within the per-step E4M3 rounding of the exact running sum."""
+    r = rng(16)
+    n, G = 4096, 128
+    main_c = np.zeros(n, np.uint8)
+    main_s = np.zeros(n // G, np.float32)
+    g = torch_bf16_bits((r.standard_normal(n) * 1e-3).astype(np.float32))
+    c1, s1 = O.fp8_accumulate(main_c, main_s, g, G, grad_dtype=O.BF16, lib=lib)
+    cq, sq = O.quantize(g, O.E4M3, G, dtype=O.BF16, lib=lib)
+    assert np.array_equal(c1, cq[:n]) and np.array_equal(s1, sq)
+    zero = np.zeros(n, np.uint16)
+    c2, s2 = O.fp8_accumulate(c1, s1, zero, G, grad_dtype=O.BF16, lib=lib)
+    assert np.array_equal(c2, c1)
+    assert np.all(np.abs(s2.view(np.int32).astype(np.int64) - s1.view(np.int32)) <= 1)
+    # each step stores D8(c)*s + g rounded once to E4M3 (up to the fp32 roundings)
+    c, s = main_c, main_s
+    for _ in range(4):
+        gi = torch_bf16_bits((r.standard_normal(n) * 1e-3).astype(np.float32))
+        prev = O.dequantize(c, s, n, O.E4M3, G, O.F32, lib=lib)
+        c, s = O.fp8_accumulate(c, s, gi, G, grad_dtype=O.BF16, lib=lib)
+        v = prev.astype(np.float64) + bf16_to_f32(gi)
+        now = O.dequantize(c, s, n, O.E4M3, G, O.F32, lib=lib)
+        ss = np.repeat(s, G).astype(np.float64)
+        assert np.all(np.abs(now - v) <= 2.0 ** -4 * np.abs(v) + 2.0 ** -10 * ss + 2.0 ** -20 * np.abs(v))
+
+
+def pin_fp8_accumulate_two_roundings(lib):
+    """v = fl(fl(D8(c) * s) + g): with D8 = 9/8, s = 1 + 2^-22 and g = -9/8 the
+    product rounds to 9/8 + 2^-22, so v = 2^-22 (a fused form gives 9 * 2^-25),
+    and the new block scale is RN32(v / 448)."""
+    n, G = 128, 128
+    codes = np.zeros(n, np.uint8)
+    codes[0] = 0x39  # E4M3 1.125
+    scales = np.array([1.0 + 2.0 ** -22], np.float32)
+    g = np.zeros(n, np.uint16)
+    g[0] = torch_bf16_bits(np.array([-1.125], np.float32))[0]
+    c, s = O.fp8_accumulate(codes, scales, g, G, grad_dtype=O.BF16, lib=lib)
+    v = rn32(rn32(Fraction(9, 8) * Fraction(float(scales[0]))) - Fraction(9, 8))
+    assert v == Fraction(2) ** -22
+    assert Fraction(float(s[0])) == rn32(v / 448)
+    assert c[0] == 0x7E and not np.any(c[1:])
+
+
+FAST_PINS = [
+    pin_bpw_endpoints, pin_bpw_formula, pin_zeropp_payload, pin_bit_layout,
+    pin_e4m3_points, pin_e4m3_vs_library, pin_f16_vs_library, pin_bf16_vs_library,
+    pin_rounding_exhaustive_16bit, pin_rounding_fractions, pin_exact_multiples_and_ties,
+    pin_zero_and_tiny_blocks, pin_e4m3_quantize, pin_block_independence, pin_roundtrip_bound,
+    pin_idempotence, pin_dequant_values, pin_reduce_single_shard, pin_reduce_pow2_exact,
+    pin_reduce_order, pin_reduce_plain_sum_and_bound, pin_reduce_two_roundings,
+    pin_fp8_reduce_no_overflow, pin_fp8_accumulate, pin_fp8_accumulate_two_roundings,
+]

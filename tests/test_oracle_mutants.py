@@ -1,0 +1,88 @@
+"""Mutation tests for the oracle's pins.
+
+Each case plants one plausible mistake in a temporary copy of the oracle's C
+source (never in the repository file), builds it, and checks that at least one
+pin from tests/pins.py fails against the broken build. A mutation that no pin
+catches would mean the pins leave that part of the oracle unchecked.
+"""
+import os
+import shutil
+import tempfile
+
+import pytest
+
+import oracle as O
+import pins
+
+SRC = os.path.join(os.path.dirname(O.__file__), "zq_oracle.c")
+
+# (name, text to find (must occur exactly once), replacement)
+MUTANTS = [
+    ("round_half_away", "float q = nearbyintf(t); /* ties to even, R3 */", "float q = roundf(t);"),
+    ("truncate_instead_of_round", "float q = nearbyintf(t); /* ties to even, R3 */", "float q = truncf(t);"),
+    ("qmax_off_by_one", "else s = m / (float)int_qmax(fmt);", "else s = m / (float)(int_qmax(fmt) + 1);"),
+    ("multiply_by_reciprocal", "float t = v[i] / s;      /* IEEE division, R4 */",
+     "float t = v[i] * (1.0f / s);"),
+    ("no_clamp", "if (q > (float)qmax) q = (float)qmax;", ""),
+    ("e4m3_wrong_max", "if (fmt == ORC_E4M3) s = m / 448.0f;", "if (fmt == ORC_E4M3) s = m / 240.0f;"),
+    ("msb_first_packing",
+     "if ((value >> k) & 1u) stream[(pos + k) >> 3] |= (uint8_t)(1u << ((pos + k) & 7));",
+     "if ((value >> k) & 1u) stream[(pos + k) >> 3] |= (uint8_t)(1u << (7 - ((pos + k) & 7)));"),
+    ("no_sign_extension", "if (c & (1u << (b - 1))) q -= (int32_t)(1u << b); /* sign extend */", ""),
+    ("wrong_scale_index", "store_elem(dst, dst_dtype, i, dequant_elem(codes, scales[i / G], fmt, i));",
+     "store_elem(dst, dst_dtype, i, dequant_elem(codes, scales[(i + 1) / G < (n + G - 1) / G ? (i + 1) / G : i / G], fmt, i));"),
+    ("reverse_shard_order", "for (r = 0; r < nshards; ++r) {", "for (r = nshards - 1; r >= 0; --r) {"),
+    ("reduce_mean", "acc = acc + d; /* one binary32 addition per shard, in shard order */",
+     "acc = acc + d / (float)nshards;"),
+    ("reduce_uses_out_block", "scales[r][(lo + i) / G_in]", "scales[r][(lo + i) / G_out]"),
+    ("reduce_fma",
+     "float d = dequant_elem(codes[r], scales[r][(lo + i) / G_in], fmt_in, lo + i);\n"
+     "                acc = acc + d; /* one binary32 addition per shard, in shard order */",
+     "acc = fmaf(dequant_elem(codes[r], 1.0f, fmt_in, lo + i), scales[r][(lo + i) / G_in], acc);"),
+    ("accumulate_fma", "float d = orc_e4m3_decode(codes[lo + i]) * scales[k];\n"
+     "            scratch[i] = d + load_elem(grad, grad_dtype, lo + i);",
+     "scratch[i] = fmaf(orc_e4m3_decode(codes[lo + i]), scales[k], load_elem(grad, grad_dtype, lo + i));"),
+    ("accumulate_drops_grad", "scratch[i] = d + load_elem(grad, grad_dtype, lo + i);", "scratch[i] = d;"),
+    ("accumulate_drops_main", "scratch[i] = d + load_elem(grad, grad_dtype, lo + i);",
+     "scratch[i] = load_elem(grad, grad_dtype, lo + i);"),
+    ("f16_subnormal_exponent", "if (ex == 0) v = ldexp((double)fr, -24);", "if (ex == 0) v = ldexp((double)fr, -25);"),
+    ("round_down_in_formats", "r = nearbyint(t);             /* default mode: nearest, ties to even */",
+     "r = floor(t);"),
+    ("e4m3_no_saturation", "if (r > 448.0) r = 448.0;", ""),
+    ("e4m3_bias_8", "else v = ldexp(8.0 + fr, ex - 10);", "else v = ldexp(8.0 + fr, ex - 11);"),
+    ("absmax_without_abs", "if (fabsf(v[i]) > m) m = fabsf(v[i]);", "if (v[i] > m) m = v[i];"),
+    ("partial_block_off_by_one",
+     "int64_t lo = k * G, len = (n - lo < G) ? n - lo : G;\n"
+     "        for (i = 0; i < len; ++i) scratch[i] = load_elem(src, dtype, lo + i);",
+     "int64_t lo = k * G, len = (n - lo < G) ? n - lo - 1 : G;\n"
+     "        for (i = 0; i < len; ++i) scratch[i] = load_elem(src, dtype, lo + i);"),
+    ("codes_not_cleared", "memset(codes, 0, (size_t)orc_codes_bytes(fmt, n));", ""),
+]
+
+
+def _first_failure(lib):
+    for pin in pins.FAST_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, ValueError, IndexError, OverflowError) as e:  # noqa: PERF203
+            return pin.__name__, e
+    return None
+
+
+@pytest.fixture(scope="module")
+def workdir():
+    d = tempfile.mkdtemp(prefix="zq_mutants_")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+@pytest.mark.parametrize("name,find,repl", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(workdir, name, find, repl):
+    text = open(SRC).read()
+    assert text.count(find) == 1, f"mutation anchor for {name} no longer matches the oracle"
+    src = os.path.join(workdir, f"{name}.c")
+    with open(src, "w") as f:
+        f.write(text.replace(find, repl))
+    lib = O.load(O.build(src=src, out=os.path.join(workdir, f"{name}.so")))
+    caught = _first_failure(lib)
+    assert caught is not None, f"no pin catches the mutation {name}"
