@@ -1,0 +1,191 @@
+"""zq -- blockwise quantize / pack / dequantize / quantized reduce / FP8 accumulate
+on one GB300 GPU.
+
+This module is a thin binding over the C ABI of ``libzq.so`` (``include/zq.h``):
+it only marshals arguments. torch supplies device memory and the current CUDA
+stream; every step of the computation runs in the library's CUDA kernels. If
+the library is missing the calls raise; there is no fallback.
+
+The operations (see ``include/zq.h`` for the exact definitions):
+  * ``quantize``          blockwise symmetric quantization to packed 2/4/6/8-bit
+                          codes or E4M3 bytes, one fp32 scale per G elements
+                          (ZeRO++ qwZ; Aquavit granularity modulation; AGoQ);
+  * ``dequantize``        codes * scale, rounded to the output type;
+  * ``reduce_quantized``  N quantized shards -> fp32 sum in shard order ->
+                          requantized (ZeRO++ qgZ; AGoQ local reduce);
+  * ``fp8_accumulate``    in-place E4M3 main-gradient update (AGoQ QuanGrad).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+F32, F16, BF16 = 0, 1, 2
+INT2, INT4, INT6, INT8, E4M3 = 2, 4, 6, 8, 0x48
+FORMATS = (INT2, INT4, INT6, INT8, E4M3)
+BLOCK_SIZES = (32, 64, 128, 256, 512, 1024)
+BITS = {INT2: 2, INT4: 4, INT6: 6, INT8: 8, E4M3: 8}
+MAX_SHARDS = 64
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libzq.so")
+
+STATUS = {0: "ZQ_OK", 1: "ZQ_ERR_INVALID_ARG", 2: "ZQ_ERR_UNSUPPORTED", 3: "ZQ_ERR_MISALIGNED",
+          4: "ZQ_ERR_ALIAS", 5: "ZQ_ERR_CUDA", 6: "ZQ_ERR_TIMEOUT"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class ZQError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        msg = f"{call} failed: {STATUS.get(status, status)}"
+        if status == 5:
+            msg += f" (cudaError {lib().zq_last_cuda_error()})"
+        super().__init__(msg)
+
+
+def _declare(L):
+    i32, i64, vp, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+    L.zq_codes_bytes.argtypes = [i32, i64]
+    L.zq_codes_bytes.restype = sz
+    L.zq_num_blocks.argtypes = [i64, i64]
+    L.zq_num_blocks.restype = i64
+    L.zq_quantize.argtypes = [vp, i32, i64, i32, i64, vp, vp, vp]
+    L.zq_dequantize.argtypes = [vp, vp, i64, i32, i64, vp, i32, vp]
+    L.zq_reduce_quantized.argtypes = [vp, vp, i32, i64, i32, i64, vp, vp, i32, i64, vp, vp]
+    L.zq_fp8_accumulate.argtypes = [vp, vp, vp, i32, i64, i64, vp]
+    for f in ("zq_quantize", "zq_dequantize", "zq_reduce_quantized", "zq_fp8_accumulate"):
+        getattr(L, f).restype = i32
+    L.zq_status_string.argtypes = [i32]
+    L.zq_status_string.restype = ctypes.c_char_p
+    L.zq_last_cuda_error.argtypes = []
+    L.zq_last_cuda_error.restype = i32
+    return L
+
+
+def lib():
+    """The loaded libzq.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"{LIB_PATH} is missing: build it with "
+                        "`python -m blockwise_quantized_zero_gb300.build` (no CPU fallback exists)")
+                _lib = _declare(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def codes_bytes(fmt: int, n: int) -> int:
+    return int(lib().zq_codes_bytes(fmt, n))
+
+
+def num_blocks(n: int, G: int) -> int:
+    return int(lib().zq_num_blocks(n, G))
+
+
+# ---------------------------------------------------------------------------
+# torch-facing wrappers (argument marshalling only)
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def dtype_code(dt) -> int:
+    torch = _torch()
+    return {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}[dt]
+
+
+def torch_dtype(code: int):
+    torch = _torch()
+    return {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}[code]
+
+
+def _stream(t, stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(status: int, call: str):
+    if status != 0:
+        raise ZQError(status, call)
+
+
+def _cuda_contig(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def empty_codes(fmt: int, n: int, device):
+    torch = _torch()
+    return torch.empty(codes_bytes(fmt, n), dtype=torch.uint8, device=device)
+
+
+def empty_scales(n: int, G: int, device):
+    torch = _torch()
+    return torch.empty(num_blocks(n, G), dtype=torch.float32, device=device)
+
+
+def quantize(src, fmt: int, G: int, codes=None, scales=None, stream=None):
+    """Quantize a CUDA tensor (fp32/fp16/bf16, flattened) -> (codes uint8, scales fp32)."""
+    _cuda_contig(src, "src")
+    n = src.numel()
+    codes = empty_codes(fmt, n, src.device) if codes is None else codes
+    scales = empty_scales(n, G, src.device) if scales is None else scales
+    _check(lib().zq_quantize(src.data_ptr(), dtype_code(src.dtype), n, fmt, G, codes.data_ptr(),
+                             scales.data_ptr(), _stream(src, stream)), "zq_quantize")
+    return codes, scales
+
+
+def dequantize(codes, scales, n: int, fmt: int, G: int, out_dtype=None, out=None, stream=None):
+    """Dequantize packed codes -> a CUDA tensor of n elements (default bf16)."""
+    torch = _torch()
+    _cuda_contig(codes, "codes")
+    if out is None:
+        out = torch.empty(n, dtype=out_dtype or torch.bfloat16, device=codes.device)
+    _check(lib().zq_dequantize(codes.data_ptr(), scales.data_ptr(), n, fmt, G, out.data_ptr(),
+                               dtype_code(out.dtype), _stream(codes, stream)), "zq_dequantize")
+    return out
+
+
+def reduce_quantized(codes_list, scales_list, n: int, fmt_in: int, G_in: int, fmt_out: int,
+                     G_out: int, out_codes=None, out_scales=None, sum_out=None, stream=None):
+    """Shard-ordered fp32 sum of N quantized shards, requantized.
+
+    ``sum_out``: None (not written), True (allocate), or an fp32 tensor of n.
+    Returns (out_codes, out_scales, sum_out_or_None)."""
+    torch = _torch()
+    N = len(codes_list)
+    if N != len(scales_list):
+        raise ValueError("codes_list and scales_list differ in length")
+    dev = codes_list[0].device
+    out_codes = empty_codes(fmt_out, n, dev) if out_codes is None else out_codes
+    out_scales = empty_scales(n, G_out, dev) if out_scales is None else out_scales
+    if sum_out is True:
+        sum_out = torch.empty(n, dtype=torch.float32, device=dev)
+    cp = (ctypes.c_void_p * N)(*[c.data_ptr() for c in codes_list])
+    sp = (ctypes.c_void_p * N)(*[s.data_ptr() for s in scales_list])
+    _check(lib().zq_reduce_quantized(cp, sp, N, n, fmt_in, G_in, out_codes.data_ptr(),
+                                     out_scales.data_ptr(), fmt_out, G_out,
+                                     sum_out.data_ptr() if sum_out is not None else None,
+                                     _stream(out_codes, stream)), "zq_reduce_quantized")
+    return out_codes, out_scales, sum_out
+
+
+def fp8_accumulate(main_codes, main_scales, grad, G: int, stream=None):
+    """In place: main (E4M3 codes + scales) <- Q8(D8(main) + grad)."""
+    _cuda_contig(grad, "grad")
+    _check(lib().zq_fp8_accumulate(main_codes.data_ptr(), main_scales.data_ptr(), grad.data_ptr(),
+                                   dtype_code(grad.dtype), grad.numel(), G,
+                                   _stream(grad, stream)), "zq_fp8_accumulate")
+    return main_codes, main_scales

@@ -1,0 +1,257 @@
+// zq_api.cu -- the C ABI of libzq (declared in include/zq.h): argument
+// validation, aliasing and device-pointer checks, and dispatch to the launch
+// units. Every argument error is reported before any work is enqueued.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "zq.h"
+#include "zq_host.h"
+
+namespace zq {
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};
+std::mutex g_sm_mutex;
+
+int bits_of(int fmt) {
+  switch (fmt) {
+    case ZQ_INT2: return 2;
+    case ZQ_INT4: return 4;
+    case ZQ_INT6: return 6;
+    case ZQ_INT8: return 8;
+    case ZQ_E4M3: return 8;
+    default: return 0;
+  }
+}
+
+int elem_bytes(int dt) {
+  switch (dt) {
+    case ZQ_F32: return 4;
+    case ZQ_F16: return 2;
+    case ZQ_BF16: return 2;
+    default: return 0;
+  }
+}
+
+bool valid_block(int64_t G) {
+  return G == 32 || G == 64 || G == 128 || G == 256 || G == 512 || G == 1024;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi)
+  Range(const void *p, size_t bytes)
+      : lo(reinterpret_cast<uintptr_t>(p)), hi(reinterpret_cast<uintptr_t>(p) + bytes) {}
+  bool overlaps(const Range &o) const { return lo < o.hi && o.lo < hi && lo != hi && o.lo != o.hi; }
+};
+
+// Device-pointer check: memory of the current device, or managed memory.
+// Disabled by setting the environment variable ZQ_CHECK_POINTERS=0.
+bool pointer_checks_enabled() {
+  static const bool on = [] {
+    const char *v = std::getenv("ZQ_CHECK_POINTERS");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
+zq_status check_device_ptr(const void *p) {
+  if (!pointer_checks_enabled()) return ZQ_OK;
+  cudaPointerAttributes attr;
+  std::memset(&attr, 0, sizeof(attr));
+  const cudaError_t e = cudaPointerGetAttributes(&attr, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    g_last_cuda_error = static_cast<int>(e);
+    return ZQ_ERR_INVALID_ARG;
+  }
+  if (attr.type == cudaMemoryTypeManaged) return ZQ_OK;
+  if (attr.type != cudaMemoryTypeDevice) return ZQ_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || attr.device != dev) {
+    (void)cudaGetLastError();
+    return ZQ_ERR_INVALID_ARG;
+  }
+  return ZQ_OK;
+}
+
+zq_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return ZQ_OK;
+  g_last_cuda_error = static_cast<int>(e);
+  return ZQ_ERR_CUDA;
+}
+
+cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    (void)cudaGetLastError();
+    return 148;
+  }
+  std::lock_guard<std::mutex> lock(g_sm_mutex);
+  if (g_sm_count[dev] == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms < 1) {
+      (void)cudaGetLastError();
+      sms = 148;
+    }
+    g_sm_count[dev] = sms;
+  }
+  return g_sm_count[dev];
+}
+
+}  // namespace zq
+
+using namespace zq;
+
+extern "C" {
+
+size_t zq_codes_bytes(int format, int64_t n) {
+  const int b = bits_of(format);
+  if (b == 0 || n < 0) return 0;
+  return static_cast<size_t>((n * b + 31) / 32) * 4u;
+}
+
+int64_t zq_num_blocks(int64_t n, int64_t G) {
+  if (n < 0 || !valid_block(G)) return 0;
+  return (n + G - 1) / G;
+}
+
+const char *zq_status_string(int status) {
+  switch (status) {
+    case ZQ_OK: return "ok";
+    case ZQ_ERR_INVALID_ARG: return "invalid argument";
+    case ZQ_ERR_UNSUPPORTED: return "unsupported format or element type";
+    case ZQ_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case ZQ_ERR_ALIAS: return "output overlaps an input";
+    case ZQ_ERR_CUDA: return "CUDA runtime error";
+    case ZQ_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int zq_last_cuda_error(void) { return g_last_cuda_error; }
+
+zq_status zq_quantize(const void *src, int src_dtype, int64_t n, int format, int64_t G, void *codes,
+                      float *scales, void *stream) {
+  if (!bits_of(format) || !elem_bytes(src_dtype)) return ZQ_ERR_UNSUPPORTED;
+  if (n < 0 || !valid_block(G)) return ZQ_ERR_INVALID_ARG;
+  if (n == 0) return ZQ_OK;
+  if (!src || !codes || !scales) return ZQ_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(codes) || !aligned16(scales)) return ZQ_ERR_MISALIGNED;
+  const Range rs(src, size_t(n) * elem_bytes(src_dtype)), rc(codes, zq_codes_bytes(format, n)),
+      rk(scales, size_t(zq_num_blocks(n, G)) * 4u);
+  if (rc.overlaps(rs) || rk.overlaps(rs) || rc.overlaps(rk)) return ZQ_ERR_ALIAS;
+  for (const void *p : {static_cast<const void *>(src), static_cast<const void *>(codes),
+                        static_cast<const void *>(scales)})
+    if (zq_status st = check_device_ptr(p)) return st;
+  const bool wide = aligned32(src);
+  return from_cuda(launch_quantize(src, src_dtype, n, format, G, codes, scales, as_stream(stream),
+                                   wide));
+}
+
+zq_status zq_dequantize(const void *codes, const float *scales, int64_t n, int format, int64_t G,
+                        void *dst, int dst_dtype, void *stream) {
+  if (!bits_of(format) || !elem_bytes(dst_dtype)) return ZQ_ERR_UNSUPPORTED;
+  if (n < 0 || !valid_block(G)) return ZQ_ERR_INVALID_ARG;
+  if (n == 0) return ZQ_OK;
+  if (!codes || !scales || !dst) return ZQ_ERR_INVALID_ARG;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(dst)) return ZQ_ERR_MISALIGNED;
+  const Range rd(dst, size_t(n) * elem_bytes(dst_dtype)), rc(codes, zq_codes_bytes(format, n)),
+      rk(scales, size_t(zq_num_blocks(n, G)) * 4u);
+  if (rd.overlaps(rc) || rd.overlaps(rk)) return ZQ_ERR_ALIAS;
+  for (const void *p : {static_cast<const void *>(codes), static_cast<const void *>(scales),
+                        static_cast<const void *>(dst)})
+    if (zq_status st = check_device_ptr(p)) return st;
+  const bool wide = aligned32(dst);
+  return from_cuda(launch_dequantize(codes, scales, n, format, G, dst, dst_dtype,
+                                     as_stream(stream), wide));
+}
+
+zq_status zq_reduce_quantized(const void *const *codes, const float *const *scales, int nshards,
+                              int64_t n, int format_in, int64_t G_in, void *out_codes,
+                              float *out_scales, int format_out, int64_t G_out, float *sum_out,
+                              void *stream) {
+  if (!bits_of(format_in) || !bits_of(format_out)) return ZQ_ERR_UNSUPPORTED;
+  if (n < 0 || !valid_block(G_in) || !valid_block(G_out) || nshards < 1 ||
+      nshards > ZQ_MAX_SHARDS)
+    return ZQ_ERR_INVALID_ARG;
+  if (n == 0) return ZQ_OK;
+  if (!codes || !scales || !out_codes || !out_scales) return ZQ_ERR_INVALID_ARG;
+  for (int r = 0; r < nshards; ++r)
+    if (!codes[r] || !scales[r]) return ZQ_ERR_INVALID_ARG;
+  for (int r = 0; r < nshards; ++r)
+    if (!aligned16(codes[r]) || !aligned16(scales[r])) return ZQ_ERR_MISALIGNED;
+  if (!aligned16(out_codes) || !aligned16(out_scales) || (sum_out && !aligned16(sum_out)))
+    return ZQ_ERR_MISALIGNED;
+  const Range oc(out_codes, zq_codes_bytes(format_out, n)),
+      os(out_scales, size_t(zq_num_blocks(n, G_out)) * 4u),
+      sm(sum_out, sum_out ? size_t(n) * 4u : 0u);
+  if (oc.overlaps(os) || oc.overlaps(sm) || os.overlaps(sm)) return ZQ_ERR_ALIAS;
+  for (int r = 0; r < nshards; ++r) {
+    const Range ic(codes[r], zq_codes_bytes(format_in, n)),
+        is(scales[r], size_t(zq_num_blocks(n, G_in)) * 4u);
+    for (const Range *o : {&oc, &os, &sm})
+      if (o->overlaps(ic) || o->overlaps(is)) return ZQ_ERR_ALIAS;
+  }
+  for (int r = 0; r < nshards; ++r) {
+    if (zq_status st = check_device_ptr(codes[r])) return st;
+    if (zq_status st = check_device_ptr(scales[r])) return st;
+  }
+  if (zq_status st = check_device_ptr(out_codes)) return st;
+  if (zq_status st = check_device_ptr(out_scales)) return st;
+  if (sum_out)
+    if (zq_status st = check_device_ptr(sum_out)) return st;
+
+  ReduceArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int r = 0; r < nshards; ++r) {
+    a.codes[r] = static_cast<const uint8_t *>(codes[r]);
+    a.scales[r] = scales[r];
+  }
+  a.out_codes = static_cast<uint8_t *>(out_codes);
+  a.out_scales = out_scales;
+  a.sum_out = sum_out;
+  a.n = n;
+  a.nshards = nshards;
+  a.log2Gin = log2_block(G_in);
+  a.log2Gout = log2_block(G_out);
+  a.wide = (!sum_out || aligned32(sum_out)) ? 1 : 0;
+  return from_cuda(launch_reduce(a, format_in, format_out, as_stream(stream)));
+}
+
+zq_status zq_fp8_accumulate(void *main_codes, float *main_scales, const void *grad, int grad_dtype,
+                            int64_t n, int64_t G, void *stream) {
+  if (!elem_bytes(grad_dtype)) return ZQ_ERR_UNSUPPORTED;
+  if (n < 0 || !valid_block(G)) return ZQ_ERR_INVALID_ARG;
+  if (n == 0) return ZQ_OK;
+  if (!main_codes || !main_scales || !grad) return ZQ_ERR_INVALID_ARG;
+  if (!aligned16(main_codes) || !aligned16(main_scales) || !aligned16(grad))
+    return ZQ_ERR_MISALIGNED;
+  const Range rc(main_codes, zq_codes_bytes(ZQ_E4M3, n)),
+      rs(main_scales, size_t(zq_num_blocks(n, G)) * 4u),
+      rg(grad, size_t(n) * elem_bytes(grad_dtype));
+  if (rc.overlaps(rs) || rg.overlaps(rc) || rg.overlaps(rs)) return ZQ_ERR_ALIAS;
+  for (const void *p : {static_cast<const void *>(main_codes),
+                        static_cast<const void *>(main_scales), grad})
+    if (zq_status st = check_device_ptr(p)) return st;
+  const bool wide = aligned32(grad);
+  return from_cuda(launch_fp8_accumulate(main_codes, main_scales, grad, grad_dtype, n, G,
+                                         as_stream(stream), wide));
+}
+
+}  // extern "C"

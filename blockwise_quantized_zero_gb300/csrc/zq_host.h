@@ -1,0 +1,52 @@
+// zq_host.h -- host-side launch plumbing shared by the libzq launch units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "zq_kernels.cuh"
+
+namespace zq {
+
+// Streaming multiprocessors of the current device (cached per device).
+int device_sm_count();
+
+// Resident CTAs per SM for one kernel instantiation (computed once).
+template <auto Kernel> int ctas_per_sm() {
+  static const int v = [] {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, Kernel, kThreads, 0) != cudaSuccess ||
+        b < 1) {
+      (void)cudaGetLastError();
+      b = 1;
+    }
+    return b;
+  }();
+  return v;
+}
+
+// Persistent grid: enough CTAs for every warp tile, at most one wave.
+template <auto Kernel> unsigned grid_for(int64_t n) {
+  const int64_t tiles = (n + kTile - 1) / kTile;
+  const int64_t ctas = (tiles + kThreads / 32 - 1) / (kThreads / 32);
+  const int64_t cap = int64_t(device_sm_count()) * ctas_per_sm<Kernel>();
+  return static_cast<unsigned>(ctas < cap ? ctas : cap);
+}
+
+// Launchers (one translation unit each). They return the launch status.
+cudaError_t launch_quantize(const void *src, int dt, int64_t n, int fmt, int64_t G, void *codes,
+                            float *scales, cudaStream_t st, bool wide);
+cudaError_t launch_dequantize(const void *codes, const float *scales, int64_t n, int fmt,
+                              int64_t G, void *dst, int dt, cudaStream_t st, bool wide);
+cudaError_t launch_reduce(const ReduceArgs &a, int fin, int fout, cudaStream_t st);
+cudaError_t launch_fp8_accumulate(void *codes, float *scales, const void *grad, int dt, int64_t n,
+                                  int64_t G, cudaStream_t st, bool wide);
+
+inline int log2_block(int64_t G) {
+  int l = 0;
+  while ((int64_t(1) << l) < G) ++l;
+  return l;
+}
+
+}  // namespace zq

@@ -1,0 +1,540 @@
+// zq_kernels.cuh -- the libzq kernels (sm_103a): quantize, dequantize,
+// quantized reduce and in-place FP8 accumulate.
+//
+// Work decomposition (all four kernels): a persistent grid of 256-thread CTAs
+// strides over "warp tiles" of 1024 consecutive elements. Lane l of a warp
+// owns the 16-element runs [e0 + j*512 + 16*l, +16) for j = 0, 1, so every
+// warp-wide load and store instruction touches one contiguous span (512 B of
+// bf16 per 256-bit load; 2*b bytes of codes per lane). Because G divides
+// 1024 and a tile starts at a multiple of 1024, a tile holds whole blocks: a
+// block of G <= 512 elements is G/16 adjacent lanes of one j, a block of 1024
+// is the whole tile. The block absmax is a shuffle tree over those lanes.
+// A tile that runs past n (at most one per call) is processed by a slower
+// warp-cooperative tail routine that handles a partial last block.
+#pragma once
+
+#include "zq_device.cuh"
+
+namespace zq {
+
+constexpr int kThreads = 256;
+constexpr int kU = 2;                      // 16-element runs per lane per tile
+constexpr int kTile = 32 * kVec * kU;      // 1024 elements per warp tile
+constexpr int kRun = 32 * kVec;            // 512 elements per warp-wide run
+
+struct WarpCursor {
+  int lane;
+  int64_t warp, nwarps;
+  __device__ __forceinline__ WarpCursor() {
+    lane = threadIdx.x & 31;
+    warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  }
+  // The partial last tile (if any) goes to the warp that would take tile
+  // n / kTile in the grid-stride order.
+  __device__ __forceinline__ bool owns_tail(int64_t n) const {
+    return (n % kTile) != 0 && warp == (n / kTile) % nwarps;
+  }
+};
+
+// ===========================================================================
+// Quantize
+// ===========================================================================
+// Block scales of one tile. Lane l computes the scale (IEEE division) and
+// its reciprocal for block l of the tile (there are 1024 / G <= 32 blocks),
+// stores it, and the values are shuffled back to the lanes of each block.
+// m[j] is the lane's block absmax for run j (already reduced over the block).
+template <int FMT, int G>
+__device__ __forceinline__ void tile_scales(const float (&m)[kU], float (&s)[kU], float (&r)[kU],
+                                            float *__restrict__ scales, int64_t e0, int lane) {
+  if constexpr (G == kTile) {
+    const float sb = block_scale<FMT>(fmaxf(m[0], m[1])), rb = safe_rcp(sb);
+    s[0] = s[1] = sb;
+    r[0] = r[1] = rb;
+    if (lane == 0) scales[e0 / G] = sb;
+  } else {
+    constexpr int L = G / kVec;          // lanes per block
+    constexpr int PER_RUN = kRun / G;    // blocks per run
+    constexpr int NB = kTile / G;        // blocks per tile
+    // gather: lane l holds the absmax of block l
+    const int src = (lane % PER_RUN) * L;
+    const float g0 = __shfl_sync(kFull, m[0], src), g1 = __shfl_sync(kFull, m[1], src);
+    const float mb = (lane < PER_RUN) ? g0 : g1;
+    const float sb = block_scale<FMT>(mb), rb = safe_rcp(sb);
+    if (lane < NB) scales[e0 / G + lane] = sb;
+    // scatter: the lanes of block (j, lane / L) fetch its scale
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const int owner = j * PER_RUN + lane / L;
+      s[j] = __shfl_sync(kFull, sb, owner);
+      r[j] = __shfl_sync(kFull, rb, owner);
+    }
+  }
+}
+
+// Runs (16 elements of one lane) that the fast path could not decide are not
+// fixed in place, where one flagged lane would hold up its whole warp; their
+// start indices go to a per-warp queue in shared memory, and the warp fixes
+// them 32 at a time, one run per lane, re-reading the source (the scale was
+// already stored). kQueue entries per warp; a flush runs when fewer than 64
+// free slots remain (one tile adds at most 64 runs).
+constexpr int kQueue = 128;
+constexpr int kWarps = kThreads / 32;
+
+// Fix the queued runs q[0 .. count): lane i takes entry base + i, re-reads
+// the source and the stored scale and code words (coherent loads: this warp
+// wrote them), patches the elements that need the exact path, and stores.
+template <int DT, int FMT, int G>
+__device__ __noinline__ void quantize_flush(const int64_t *q, int count,
+                                            const void *__restrict__ src,
+                                            uint8_t *__restrict__ codes, const float *scales,
+                                            int lane, bool wide) {
+  constexpr int B = Fmt<FMT>::kBits, W = Fmt<FMT>::kWords16;
+  __syncwarp();  // queue entries, scales and fast-path codes of all lanes are visible
+  for (int base = 0; base < count; base += 32) {
+    const int i = base + lane;
+    if (i < count) {
+      const int64_t e = q[i];
+      uint32_t raw[kRawWords<DT>];
+      float x[kVec];
+      load16_raw<DT>(src, e, raw, wide);
+      widen16<DT>(raw, x);
+      const float s = scales[e / G];
+      const float r = safe_rcp(s);
+      uint8_t *cp = codes + e * B / 8;
+      uint32_t w[W];
+      const bool normal = (FMT == F_E4M3) ? scale_is_normal(s) : (s == 0.0f || scale_is_normal(s));
+      if (normal && FMT != F_E4M3) {
+        quant16_fix<FMT>(x, s, r, 1u, w);  // recomputes the run; needs no old words
+      } else if (normal) {
+        if constexpr (B == 2) {
+          w[0] = *reinterpret_cast<const uint32_t *>(cp);
+        } else if constexpr (B == 4) {
+          const uint2 v = *reinterpret_cast<const uint2 *>(cp);
+          w[0] = v.x;
+          w[1] = v.y;
+        } else if constexpr (B == 6) {
+          const uint32_t *p = reinterpret_cast<const uint32_t *>(cp);
+          w[0] = p[0];
+          w[1] = p[1];
+          w[2] = p[2];
+        } else {
+          ld_v4(cp, w[0], w[1], w[2], w[3]);
+        }
+        quant16_fix<FMT>(x, s, r, 1u, w);
+      } else {
+        quant16_exact<FMT>(x, s, w);
+      }
+      store_codes16<B>(cp, w);
+    }
+  }
+  __syncwarp();
+}
+
+template <int DT, int FMT, int G>
+__device__ __forceinline__ void quantize_tile(const uint32_t (&raw)[kU][kRawWords<DT>],
+                                              uint8_t *__restrict__ codes,
+                                              float *__restrict__ scales, int64_t e0, int lane,
+                                              int64_t *q, int &count) {
+  constexpr int B = Fmt<FMT>::kBits, W = Fmt<FMT>::kWords16;
+  float x[kU][kVec];
+  float m[kU];
+#pragma unroll
+  for (int j = 0; j < kU; ++j) {
+    widen16<DT>(raw[j], x[j]);
+    m[j] = absmax16_raw<DT>(raw[j], x[j]);
+  }
+  if constexpr (G <= kRun) {
+#pragma unroll
+    for (int j = 0; j < kU; ++j) m[j] = group_max<G / kVec>(m[j]);
+  } else {
+    m[0] = m[1] = warp_max(fmaxf(m[0], m[1]));
+  }
+  float s[kU], r[kU];
+  tile_scales<FMT, G>(m, s, r, scales, e0, lane);
+
+#pragma unroll
+  for (int j = 0; j < kU; ++j) {
+    uint32_t w[W];
+    const int64_t e = e0 + j * kRun + lane * kVec;
+    const uint32_t flagged = quant16_try_fast<FMT>(x[j], s[j], r[j], w);
+    store_codes16<B>(codes + e * B / 8, w);
+    const unsigned ballot = __ballot_sync(kFull, flagged != 0u);
+    if (ballot) {
+      if (flagged) q[count + __popc(ballot & ((1u << lane) - 1u))] = e;
+      count += __popc(ballot);
+    }
+  }
+}
+
+// Exact, warp-cooperative quantization of elements [e0, n) (fewer than one
+// tile; e0 is a multiple of G). Each lane builds whole 32-bit code words.
+template <int DT, int FMT, int G>
+__device__ __noinline__ void quantize_tail(const void *__restrict__ src,
+                                           uint8_t *__restrict__ codes,
+                                           float *__restrict__ scales, int64_t e0, int64_t n,
+                                           int lane) {
+  constexpr int B = Fmt<FMT>::kBits;
+  uint32_t *cw = reinterpret_cast<uint32_t *>(codes);
+  for (int64_t lo = e0; lo < n; lo += G) {
+    const int64_t hi = (lo + G < n) ? lo + G : n;
+    float m = 0.0f;
+    for (int64_t i = lo + lane; i < hi; i += 32) m = fmaxf(m, fabsf(load1_f32<DT>(src, i)));
+    const float s = block_scale<FMT>(warp_max(m));
+    if (lane == 0) scales[lo / G] = s;
+    const int64_t len = hi - lo, nwords = (len * B + 31) / 32, w0 = lo * B / 32;
+    for (int64_t wi = lane; wi < nwords; wi += 32) {
+      const int64_t bit0 = wi * 32;
+      const int64_t first = bit0 / B;
+      const int64_t last = ((bit0 + 32 + B - 1) / B < len) ? (bit0 + 32 + B - 1) / B : len;
+      uint32_t word = 0;
+      for (int64_t e = first; e < last; ++e) {
+        const uint32_t c = code1_exact<FMT>(load1_f32<DT>(src, lo + e), s);
+        const int sh = static_cast<int>(e * B - bit0);
+        word |= (sh >= 0) ? (c << sh) : (c >> (-sh));
+      }
+      cw[w0 + wi] = word;
+    }
+  }
+}
+
+template <int DT, int FMT, int G>
+__global__ void __launch_bounds__(kThreads, 3) quantize_kernel(const void *__restrict__ src,
+                                                            uint8_t *__restrict__ codes,
+                                                            float *__restrict__ scales,
+                                                            int64_t n, int wide) {
+  const WarpCursor c;
+  const int64_t nfull = n / kTile;
+  const bool wd = wide != 0;
+  __shared__ int64_t queue[kWarps][kQueue];
+  int64_t *q = queue[threadIdx.x >> 5];
+  int count = 0;  // warp-uniform
+  // Software pipeline: the loads of tile t + nwarps are in flight while
+  // tile t is quantized.
+  uint32_t raw[kU][kRawWords<DT>];
+  int64_t t = c.warp;
+  if (t < nfull) {
+#pragma unroll
+    for (int j = 0; j < kU; ++j) load16_raw<DT>(src, t * kTile + j * kRun + c.lane * kVec, raw[j], wd);
+  }
+  for (; t < nfull; t += c.nwarps) {
+    uint32_t cur[kU][kRawWords<DT>];
+#pragma unroll
+    for (int j = 0; j < kU; ++j)
+#pragma unroll
+      for (int k = 0; k < kRawWords<DT>; ++k) cur[j][k] = raw[j][k];
+    const int64_t tn = t + c.nwarps;
+    if (tn < nfull) {
+#pragma unroll
+      for (int j = 0; j < kU; ++j)
+        load16_raw<DT>(src, tn * kTile + j * kRun + c.lane * kVec, raw[j], wd);
+    }
+    quantize_tile<DT, FMT, G>(cur, codes, scales, t * kTile, c.lane, q, count);
+    if (count > kQueue - 2 * 32) {
+      quantize_flush<DT, FMT, G>(q, count, src, codes, scales, c.lane, wd);
+      count = 0;
+    }
+  }
+  if (count) quantize_flush<DT, FMT, G>(q, count, src, codes, scales, c.lane, wd);
+  if (c.owns_tail(n)) quantize_tail<DT, FMT, G>(src, codes, scales, nfull * kTile, n, c.lane);
+}
+
+// ===========================================================================
+// Dequantize
+// ===========================================================================
+template <int FMT, int DT>
+__global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t *__restrict__ codes,
+                                                              const float *__restrict__ scales,
+                                                              void *__restrict__ dst, int64_t n,
+                                                              int log2G, int wide) {
+  constexpr int B = Fmt<FMT>::kBits, W = Fmt<FMT>::kWords16;
+  const WarpCursor c;
+  const int64_t nfull = n / kTile;
+  const bool wd = wide != 0;
+  // Software pipeline: codes and scales of tile t + nwarps are loaded while
+  // tile t is decoded and stored.
+  uint32_t w[kU][W];
+  float s[kU];
+  int64_t t = c.warp;
+  auto load = [&](int64_t tile) {
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const int64_t e = tile * kTile + j * kRun + c.lane * kVec;
+      load_codes16<B>(codes + e * B / 8, w[j]);
+      s[j] = ld_nc_f32(scales + (e >> log2G));
+    }
+  };
+  if (t < nfull) load(t);
+  for (; t < nfull; t += c.nwarps) {
+    uint32_t wc[kU][W];
+    float sc[kU];
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      sc[j] = s[j];
+#pragma unroll
+      for (int k = 0; k < W; ++k) wc[j][k] = w[j][k];
+    }
+    if (t + c.nwarps < nfull) load(t + c.nwarps);
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      float y[kVec];
+      dequant16<FMT>(wc[j], sc[j], y);
+      store16<DT>(dst, t * kTile + j * kRun + c.lane * kVec, y, wd);
+    }
+  }
+  if (c.owns_tail(n)) {
+    for (int64_t i = nfull * kTile + c.lane; i < n; i += 32)
+      store1<DT>(dst, i, dequant1<FMT>(codes, i, scales[i >> log2G]));
+  }
+}
+
+// ===========================================================================
+// Quantized reduce: acc = +0; acc = fl(acc + fl(D(shard r))) for r in order;
+// then requantize acc with (FOUT, Gout).
+// ===========================================================================
+constexpr int kMaxShards = 64;
+
+struct ReduceArgs {
+  const uint8_t *codes[kMaxShards];
+  const float *scales[kMaxShards];
+  uint8_t *out_codes;
+  float *out_scales;
+  float *sum_out;
+  int64_t n;
+  int nshards;
+  int log2Gin;
+  int log2Gout;
+  int wide;
+};
+
+// Add shard r's 16 dequantized values into acc (one binary32 add each).
+// The adds are scalar add.rn.f32 on purpose: ptxas contracts a packed
+// mul.rn.f32x2 feeding a packed add.rn.f32x2 into a fused multiply-add (even
+// with the explicit .rn and -fmad=false), which would skip the rounding of the
+// product that the definition requires; scalar add.rn.f32 is never contracted.
+template <int FIN>
+__device__ __forceinline__ void accumulate16(float (&acc)[kVec],
+                                             const uint32_t (&w)[Fmt<FIN>::kWords16], float s) {
+  float d[kVec];
+  dequant16<FIN>(w, s, d);
+#pragma unroll
+  for (int v = 0; v < kVec; ++v) acc[v] = __fadd_rn(acc[v], d[v]);
+}
+
+template <int FOUT>
+__device__ __forceinline__ void requant_tile(const ReduceArgs &a, float (&acc)[kU][kVec],
+                                             int64_t e0, int lane) {
+  constexpr int B = Fmt<FOUT>::kBits, W = Fmt<FOUT>::kWords16;
+  const int Gout = 1 << a.log2Gout;
+  float s[kU], r[kU];
+  if (Gout <= kRun) {
+    const int L = Gout / kVec;
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      s[j] = block_scale<FOUT>(group_max_rt(absmax16(acc[j]), L));
+      r[j] = safe_rcp(s[j]);
+      if ((lane & (L - 1)) == 0) a.out_scales[(e0 + j * kRun + lane * kVec) >> a.log2Gout] = s[j];
+    }
+  } else {
+    const float m = warp_max(fmaxf(absmax16(acc[0]), absmax16(acc[1])));
+    s[0] = s[1] = block_scale<FOUT>(m);
+    r[0] = r[1] = safe_rcp(s[0]);
+    if (lane == 0) a.out_scales[e0 >> a.log2Gout] = s[0];
+  }
+  uint32_t w[kU][W];
+#pragma unroll
+  for (int j = 0; j < kU; ++j) {
+    const uint32_t flagged = quant16_try_fast<FOUT>(acc[j], s[j], r[j], w[j]);
+    if (flagged) quant16_fix<FOUT>(acc[j], s[j], r[j], flagged, w[j]);
+  }
+#pragma unroll
+  for (int j = 0; j < kU; ++j)
+    store_codes16<B>(a.out_codes + (e0 + j * kRun + lane * kVec) * B / 8, w[j]);
+}
+
+// Sum over shards of element i (tails).
+template <int FIN> __device__ __forceinline__ float reduce1(const ReduceArgs &a, int64_t i) {
+  float acc = 0.0f;
+  for (int r = 0; r < a.nshards; ++r)
+    acc = __fadd_rn(acc, dequant1<FIN>(a.codes[r], i, a.scales[r][i >> a.log2Gin]));
+  return acc;
+}
+
+template <int FIN, int FOUT>
+__device__ __noinline__ void reduce_tail(const ReduceArgs &a, int64_t e0, int lane) {
+  constexpr int B = Fmt<FOUT>::kBits;
+  const int64_t n = a.n, Gout = int64_t(1) << a.log2Gout;
+  uint32_t *cw = reinterpret_cast<uint32_t *>(a.out_codes);
+  for (int64_t lo = e0; lo < n; lo += Gout) {
+    const int64_t hi = (lo + Gout < n) ? lo + Gout : n;
+    float m = 0.0f;
+    for (int64_t i = lo + lane; i < hi; i += 32) {
+      const float v = reduce1<FIN>(a, i);
+      if (a.sum_out) a.sum_out[i] = v;
+      m = fmaxf(m, fabsf(v));
+    }
+    const float s = block_scale<FOUT>(warp_max(m));
+    if (lane == 0) a.out_scales[lo >> a.log2Gout] = s;
+    const int64_t len = hi - lo, nwords = (len * B + 31) / 32, w0 = lo * B / 32;
+    for (int64_t wi = lane; wi < nwords; wi += 32) {
+      const int64_t bit0 = wi * 32, first = bit0 / B;
+      const int64_t last = ((bit0 + 32 + B - 1) / B < len) ? (bit0 + 32 + B - 1) / B : len;
+      uint32_t word = 0;
+      for (int64_t e = first; e < last; ++e) {
+        const uint32_t c = code1_exact<FOUT>(reduce1<FIN>(a, lo + e), s);
+        const int sh = static_cast<int>(e * B - bit0);
+        word |= (sh >= 0) ? (c << sh) : (c >> (-sh));
+      }
+      cw[w0 + wi] = word;
+    }
+  }
+}
+
+template <int FIN, int FOUT>
+__global__ void __launch_bounds__(kThreads) reduce_kernel(const __grid_constant__ ReduceArgs a) {
+  constexpr int BIN = Fmt<FIN>::kBits, WIN = Fmt<FIN>::kWords16;
+  constexpr int kBatch = 4;  // shards whose loads are in flight together
+  const WarpCursor c;
+  const int64_t nfull = a.n / kTile;
+  for (int64_t t = c.warp; t < nfull; t += c.nwarps) {
+    const int64_t e0 = t * kTile;
+    float acc[kU][kVec];
+#pragma unroll
+    for (int j = 0; j < kU; ++j)
+#pragma unroll
+      for (int v = 0; v < kVec; ++v) acc[j][v] = 0.0f;
+
+    int r = 0;
+    for (; r + kBatch <= a.nshards; r += kBatch) {
+      uint32_t w[kBatch][kU][WIN];
+      float s[kBatch][kU];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+#pragma unroll
+        for (int j = 0; j < kU; ++j) {
+          const int64_t e = e0 + j * kRun + c.lane * kVec;
+          load_codes16<BIN>(a.codes[r + k] + e * BIN / 8, w[k][j]);
+          s[k][j] = ld_nc_f32(a.scales[r + k] + (e >> a.log2Gin));
+        }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+#pragma unroll
+        for (int j = 0; j < kU; ++j) accumulate16<FIN>(acc[j], w[k][j], s[k][j]);
+    }
+    for (; r < a.nshards; ++r) {
+      uint32_t w[kU][WIN];
+      float s[kU];
+#pragma unroll
+      for (int j = 0; j < kU; ++j) {
+        const int64_t e = e0 + j * kRun + c.lane * kVec;
+        load_codes16<BIN>(a.codes[r] + e * BIN / 8, w[j]);
+        s[j] = ld_nc_f32(a.scales[r] + (e >> a.log2Gin));
+      }
+#pragma unroll
+      for (int j = 0; j < kU; ++j) accumulate16<FIN>(acc[j], w[j], s[j]);
+    }
+    if (a.sum_out) {
+#pragma unroll
+      for (int j = 0; j < kU; ++j)
+        store16<DT_F32>(a.sum_out, e0 + j * kRun + c.lane * kVec, acc[j], a.wide != 0);
+    }
+    requant_tile<FOUT>(a, acc, e0, c.lane);
+  }
+  if (c.owns_tail(a.n)) reduce_tail<FIN, FOUT>(a, nfull * kTile, c.lane);
+}
+
+// ===========================================================================
+// FP8 accumulate, in place: v = fl(fl(e4m3(c) * s) + g); requantize to E4M3.
+// Each warp reads and rewrites only its own tile (codes and block scales),
+// and every lane reads the old scale before the block-max shuffle that
+// precedes the new scale's store, so the in-place update is race free.
+// ===========================================================================
+template <int DT, int G>
+__device__ __forceinline__ void fp8acc_tile(uint8_t *codes, float *scales,
+                                            const void *__restrict__ grad, int64_t e0, int lane,
+                                            bool wide) {
+  float v[kU][kVec];
+  uint32_t w[kU][4];
+  float sold[kU];
+#pragma unroll
+  for (int j = 0; j < kU; ++j) {
+    const int64_t e = e0 + j * kRun + lane * kVec;
+    ld_v4(codes + e, w[j][0], w[j][1], w[j][2], w[j][3]);
+    sold[j] = scales[e / G];
+    load16_f32<DT>(grad, e, v[j], wide);
+  }
+#pragma unroll
+  for (int j = 0; j < kU; ++j) {
+    float d[kVec];
+    dequant16<F_E4M3>(w[j], sold[j], d);
+    // scalar adds: see accumulate16 (a packed add after the packed product
+    // would be fused with it)
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) v[j][k] = __fadd_rn(d[k], v[j][k]);
+  }
+  float s[kU], r[kU];
+  if constexpr (G <= kRun) {
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      s[j] = block_scale<F_E4M3>(group_max<G / kVec>(absmax16(v[j])));
+      r[j] = safe_rcp(s[j]);
+      if ((lane & (G / kVec - 1)) == 0) scales[(e0 + j * kRun + lane * kVec) / G] = s[j];
+    }
+  } else {
+    const float m = warp_max(fmaxf(absmax16(v[0]), absmax16(v[1])));
+    s[0] = s[1] = block_scale<F_E4M3>(m);
+    r[0] = r[1] = safe_rcp(s[0]);
+    if (lane == 0) scales[e0 / G] = s[0];
+  }
+#pragma unroll
+  for (int j = 0; j < kU; ++j) {
+    const uint32_t flagged = quant16_try_fast<F_E4M3>(v[j], s[j], r[j], w[j]);
+    if (flagged) quant16_fix<F_E4M3>(v[j], s[j], r[j], flagged, w[j]);
+  }
+#pragma unroll
+  for (int j = 0; j < kU; ++j)
+    st_v4(codes + e0 + j * kRun + lane * kVec, w[j][0], w[j][1], w[j][2], w[j][3]);
+}
+
+template <int DT, int G>
+__device__ __noinline__ void fp8acc_tail(uint8_t *codes, float *scales,
+                                         const void *__restrict__ grad, int64_t e0, int64_t n,
+                                         int lane) {
+  for (int64_t lo = e0; lo < n; lo += G) {
+    const int64_t hi = (lo + G < n) ? lo + G : n;
+    const float sold = scales[lo / G];
+    float m = 0.0f;
+    for (int64_t i = lo + lane; i < hi; i += 32)
+      m = fmaxf(m, fabsf(__fadd_rn(__fmul_rn(f32_from_e4m3(codes[i]), sold),
+                                   load1_f32<DT>(grad, i))));
+    const float s = block_scale<F_E4M3>(warp_max(m));
+    // every lane has read `sold` and the old codes of its words before any
+    // lane writes: the codes of one word are read and written by one lane
+    const int64_t len = hi - lo, nwords = (len + 3) / 4;
+    uint32_t *cw = reinterpret_cast<uint32_t *>(codes + lo);
+    for (int64_t wi = lane; wi < nwords; wi += 32) {
+      uint32_t word = 0;
+      for (int k = 0; k < 4 && wi * 4 + k < len; ++k) {
+        const int64_t i = lo + wi * 4 + k;
+        const float vi = __fadd_rn(__fmul_rn(f32_from_e4m3(codes[i]), sold), load1_f32<DT>(grad, i));
+        word |= code_e4m3_exact(vi, s) << (8 * k);
+      }
+      cw[wi] = word;
+    }
+    __syncwarp();
+    if (lane == 0) scales[lo / G] = s;
+  }
+}
+
+template <int DT, int G>
+__global__ void __launch_bounds__(kThreads) fp8_accumulate_kernel(uint8_t *codes, float *scales,
+                                                                  const void *__restrict__ grad,
+                                                                  int64_t n, int wide) {
+  const WarpCursor c;
+  const int64_t nfull = n / kTile;
+  for (int64_t t = c.warp; t < nfull; t += c.nwarps)
+    fp8acc_tile<DT, G>(codes, scales, grad, t * kTile, c.lane, wide != 0);
+  if (c.owns_tail(n)) fp8acc_tail<DT, G>(codes, scales, grad, nfull * kTile, n, c.lane);
+}
+
+}  // namespace zq

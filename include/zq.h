@@ -1,0 +1,166 @@
+/*
+ * zq.h -- C ABI of libzq: blockwise quantize / pack / dequantize /
+ * quantized-reduce / FP8-accumulate kernels for one GB300 GPU (sm_103a).
+ *
+ * The operations follow these pages:
+ *  [ZeRO++]  "Quantized LLM Training at Scale with ZeRO++" -- section "Blockwise
+ *            weight quantization cuts forward-gather traffic in half" (qwZ:
+ *            weights split into blocks, 8-bit codes with a scale per block) and
+ *            section "QGZ keeps reductions in full precision while sending
+ *            quantized gradients" (qgZ: 4/8-bit gradients dequantized, summed in
+ *            full precision, requantized once);
+ *  [Aquavit] "Aquavit: Ascending Quantization for Communication-Efficient
+ *            Vast-Scale Distributed Training" (review) -- granularity
+ *            modulation, Eq. 6 / Table 1: b in {2,4,6,8}, 32 bits of metadata
+ *            per G-element block, bpw = b + 32/G;
+ *  [AGoQ]    "AGoQ: Activation and Gradient Quantization for Memory-Efficient
+ *            Distributed Training of LLMs" -- section 2.B (QuanGrad): "Local
+ *            Accumulation" and the "Local Reduce" step of the precision-
+ *            preserved all-reduce.
+ *
+ * ----------------------------------------------------------------------------
+ * Data layout (identical for every call)
+ * ----------------------------------------------------------------------------
+ *  - A tensor is a flat array of n elements; blocks are G consecutive elements
+ *    (G in {32, 64, 128, 256, 512, 1024}); the last block may be partial.
+ *  - scales: one fp32 per block, nb = ceil(n / G) of them, in block order,
+ *    scale = absmax(block) / qmax with qmax = 2^(b-1) - 1 (1, 7, 31, 127), or
+ *    absmax / 448 for E4M3. A block whose scale is 0 has all-zero codes.
+ *  - codes: integer code q = clamp(rint(x / scale), -qmax, qmax) (IEEE binary32
+ *    division, ties to even) stored as b-bit two's complement; code i occupies
+ *    bits [i*b, i*b + b) of a little-endian stream of 32-bit words (LSB first;
+ *    6-bit codes straddle words). E4M3 codes are one byte each, the nearest
+ *    E4M3 value of x / scale (ties to even, saturating at +-448). The stream
+ *    is zq_codes_bytes(format, n) bytes long; unused trailing bits are zero.
+ *  - Dequantized value: fl32(q * scale) (or fl32(e4m3(q) * scale)), then one
+ *    round-to-nearest-even to the output type.
+ *
+ * ----------------------------------------------------------------------------
+ * Conventions
+ * ----------------------------------------------------------------------------
+ *  - Every data pointer is a DEVICE pointer (memory the GPU can address, e.g.
+ *    from cudaMalloc or a torch CUDA tensor), 16-byte aligned, owned by the
+ *    caller. The library allocates nothing and never synchronizes: work is
+ *    enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ *    and the call returns. Pointer arrays (shards) are HOST arrays, read
+ *    during the call only.
+ *  - Argument errors return synchronously with no work enqueued. A failed
+ *    launch returns ZQ_ERR_CUDA; zq_last_cuda_error() then gives the CUDA
+ *    runtime error code (per host thread). Errors that occur later on the
+ *    device surface through the usual CUDA stream error reporting.
+ *  - Outputs must not overlap inputs (ZQ_ERR_ALIAS), except the documented
+ *    in-place update of zq_fp8_accumulate.
+ *  - NaN and infinite inputs are outside the contract.
+ *  - n = 0 is valid and enqueues nothing.
+ *  - The calls are thread-safe: they keep no state between calls except
+ *    per-device launch parameters computed on first use.
+ */
+#ifndef ZQ_H
+#define ZQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum zq_status {
+    ZQ_OK = 0,
+    ZQ_ERR_INVALID_ARG = 1, /* null pointer, n < 0, bad block size, bad shard count */
+    ZQ_ERR_UNSUPPORTED = 2, /* unknown format or element type */
+    ZQ_ERR_MISALIGNED = 3,  /* a data pointer is not 16-byte aligned */
+    ZQ_ERR_ALIAS = 4,       /* an output overlaps an input */
+    ZQ_ERR_CUDA = 5,        /* the CUDA runtime reported an error (see zq_last_cuda_error) */
+    ZQ_ERR_TIMEOUT = 6      /* reserved: a bounded device-side wait ran out */
+} zq_status;
+
+/* Element types of uncompressed tensors. */
+typedef enum zq_dtype { ZQ_F32 = 0, ZQ_F16 = 1, ZQ_BF16 = 2 } zq_dtype;
+
+/* Code formats: the value is the integer bit width, except E4M3. */
+typedef enum zq_format {
+    ZQ_INT2 = 2,
+    ZQ_INT4 = 4,
+    ZQ_INT6 = 6,
+    ZQ_INT8 = 8,
+    ZQ_E4M3 = 0x48
+} zq_format;
+
+/* Largest shard count accepted by zq_reduce_quantized. */
+#define ZQ_MAX_SHARDS 64
+
+/* Bytes of the packed code stream for n elements: ceil(n * bits / 32) * 4.
+ * With n a multiple of G this is n * b / 8 ([Aquavit] Eq. 6 without the
+ * metadata term). Returns 0 for an unknown format or n < 0. Host only. */
+size_t zq_codes_bytes(int format, int64_t n);
+
+/* Number of blocks, ceil(n / G); 0 for an invalid G or n < 0. Host only. */
+int64_t zq_num_blocks(int64_t n, int64_t G);
+
+/*
+ * zq_quantize -- blockwise symmetric quantization ([ZeRO++] qwZ section;
+ * [Aquavit] Eq. 6 for b in {2,4,6,8}; [AGoQ] 2.B for E4M3).
+ *   src      device, n elements of src_dtype (ZQ_F32 / ZQ_F16 / ZQ_BF16)
+ *   format   ZQ_INT2 / ZQ_INT4 / ZQ_INT6 / ZQ_INT8 / ZQ_E4M3
+ *   G        block size, a power of two in [32, 1024]
+ *   codes    device, zq_codes_bytes(format, n) bytes, written in full
+ *   scales   device, zq_num_blocks(n, G) floats, written in full
+ * Results are bit-identical to the definition in the layout section above.
+ */
+zq_status zq_quantize(const void *src, int src_dtype, int64_t n, int format, int64_t G, void *codes,
+                      float *scales, void *stream);
+
+/*
+ * zq_dequantize -- inverse of zq_quantize ([ZeRO++] qwZ: dequantize after the
+ * gather; qgZ: dequantize before the full-precision reduction).
+ *   codes, scales  device, as written by zq_quantize(format, G)
+ *   dst            device, n elements of dst_dtype, written in full
+ */
+zq_status zq_dequantize(const void *codes, const float *scales, int64_t n, int format, int64_t G,
+                        void *dst, int dst_dtype, void *stream);
+
+/*
+ * zq_reduce_quantized -- quantized gradient reduce ([ZeRO++] qgZ section:
+ * dequantize, reduce in full precision, requantize once; [AGoQ] 2.B "Local
+ * Reduce": FP8 shards dequantized to FP32, summed, requantized to FP8).
+ * For every element i:  acc = +0.0f;  for r = 0 .. nshards-1 in order:
+ * acc = fl32(acc + fl32(D(shard r, i)));  then acc is quantized with
+ * (format_out, G_out) exactly as zq_quantize would. The sum is not averaged.
+ *   codes[r], scales[r]  device pointers held in HOST arrays of nshards
+ *                        entries; shard r in (format_in, G_in) layout
+ *   nshards              1 .. ZQ_MAX_SHARDS
+ *   out_codes, out_scales  device, (format_out, G_out) layout
+ *   sum_out              device, n floats (the fp32 sums), or NULL
+ * Results are bit-identical to the definition (the shard order is kept).
+ */
+zq_status zq_reduce_quantized(const void *const *codes, const float *const *scales, int nshards,
+                              int64_t n, int format_in, int64_t G_in, void *out_codes,
+                              float *out_scales, int format_out, int64_t G_out, float *sum_out,
+                              void *stream);
+
+/*
+ * zq_fp8_accumulate -- in-place FP8 gradient accumulation ([AGoQ] 2.B "Local
+ * Accumulation", with the addition in fp32):
+ *   v_i = fl32(fl32(e4m3(c_i) * s_block) + g_i), then the block is requantized
+ *   to E4M3 with a new scale absmax(v)/448, overwriting codes and scales.
+ *   main_codes   device, n E4M3 bytes (zq_codes_bytes(ZQ_E4M3, n) bytes), in place
+ *   main_scales  device, zq_num_blocks(n, G) floats, in place
+ *   grad         device, n elements of grad_dtype; must not overlap the main gradient
+ * A main gradient of all-zero codes and zero scales is the empty accumulator.
+ */
+zq_status zq_fp8_accumulate(void *main_codes, float *main_scales, const void *grad, int grad_dtype,
+                            int64_t n, int64_t G, void *stream);
+
+/* Static description of a status code. */
+const char *zq_status_string(int status);
+
+/* CUDA runtime error code (cudaError_t) behind the last ZQ_ERR_CUDA returned
+ * on the calling host thread; 0 if none. */
+int zq_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZQ_H */

@@ -1,0 +1,127 @@
+"""The C ABI without a GPU: libzq.so loads, exports every symbol declared in
+include/zq.h, and rejects every bad argument before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import blockwise_quantized_zero_gb300 as zq
+import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "zq.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, ALIAS = 0, 1, 2, 3, 4
+BASE = 0x7F0000000000  # fake device addresses: never dereferenced by these calls
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(zq_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    return zq.lib()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for f in ("zq_quantize", "zq_dequantize", "zq_reduce_quantized", "zq_fp8_accumulate",
+              "zq_codes_bytes", "zq_num_blocks", "zq_status_string", "zq_last_cuda_error"):
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_size_helpers_match_the_oracle(L):
+    for fmt in zq.FORMATS:
+        for n in (0, 1, 31, 32, 33, 1000, 1 << 20, 67108864 + 5):
+            assert zq.codes_bytes(fmt, n) == O.codes_bytes(fmt, n)
+    for G in zq.BLOCK_SIZES:
+        for n in (0, 1, G - 1, G, G + 1, 855638016):
+            assert zq.num_blocks(n, G) == O.num_blocks(n, G)
+    assert zq.codes_bytes(3, 10) == 0 and zq.codes_bytes(zq.INT4, -1) == 0
+    assert zq.num_blocks(10, 48) == 0 and zq.num_blocks(-1, 32) == 0
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert L.zq_status_string(s)
+    assert L.zq_last_cuda_error() == 0
+
+
+def q(L, src=BASE, dt=zq.BF16, n=4096, fmt=zq.INT8, G=256, codes=BASE + (1 << 24),
+      scales=BASE + (1 << 26)):
+    return L.zq_quantize(src, dt, n, fmt, G, codes, scales, None)
+
+
+def test_quantize_argument_errors(L):
+    assert q(L, fmt=3) == UNSUPPORTED
+    assert q(L, dt=7) == UNSUPPORTED
+    assert q(L, n=-1) == INVALID
+    assert q(L, G=48) == INVALID and q(L, G=16) == INVALID and q(L, G=2048) == INVALID
+    assert q(L, n=0, src=None, codes=None, scales=None) == OK  # empty: nothing to do
+    assert q(L, src=None) == INVALID and q(L, codes=None) == INVALID and q(L, scales=None) == INVALID
+    assert q(L, src=BASE + 8) == MISALIGNED and q(L, codes=BASE + (1 << 24) + 4) == MISALIGNED
+    assert q(L, scales=BASE + (1 << 26) + 2) == MISALIGNED
+    assert q(L, codes=BASE + 4096) == ALIAS  # codes inside the 8 KiB source
+    assert q(L, scales=BASE + (1 << 24) + 1024) == ALIAS  # scales inside the codes
+
+
+def test_dequantize_argument_errors(L):
+    c, s, d = BASE, BASE + (1 << 24), BASE + (1 << 26)
+    assert L.zq_dequantize(c, s, 4096, 5, 256, d, zq.BF16, None) == UNSUPPORTED
+    assert L.zq_dequantize(c, s, 4096, zq.INT4, 256, d, 9, None) == UNSUPPORTED
+    assert L.zq_dequantize(c, s, -5, zq.INT4, 256, d, zq.BF16, None) == INVALID
+    assert L.zq_dequantize(c, s, 4096, zq.INT4, 100, d, zq.BF16, None) == INVALID
+    assert L.zq_dequantize(None, s, 4096, zq.INT4, 256, d, zq.BF16, None) == INVALID
+    assert L.zq_dequantize(c, s, 4096, zq.INT4, 256, d + 16 + 8, zq.BF16, None) == MISALIGNED
+    assert L.zq_dequantize(c, s, 4096, zq.INT4, 256, c + 512, zq.BF16, None) == ALIAS
+    assert L.zq_dequantize(c, s, 0, zq.INT4, 256, d, zq.BF16, None) == OK
+
+
+def test_reduce_argument_errors(L):
+    N, n = 4, 4096
+    cp = (ctypes.c_void_p * N)(*[BASE + i * (1 << 20) for i in range(N)])
+    sp = (ctypes.c_void_p * N)(*[BASE + (1 << 28) + i * (1 << 20) for i in range(N)])
+    oc, os_, sm = BASE + (1 << 30), BASE + (1 << 31), BASE + (1 << 32)
+
+    def r(**kw):
+        a = dict(codes=cp, scales=sp, N=N, n=n, fin=zq.INT4, Gin=128, oc=oc, os=os_, fout=zq.INT4,
+                 Gout=128, sm=sm)
+        a.update(kw)
+        return L.zq_reduce_quantized(a["codes"], a["scales"], a["N"], a["n"], a["fin"], a["Gin"],
+                                     a["oc"], a["os"], a["fout"], a["Gout"], a["sm"], None)
+
+    assert r(fin=1) == UNSUPPORTED and r(fout=0x49) == UNSUPPORTED
+    assert r(N=0) == INVALID and r(N=65) == INVALID
+    assert r(Gin=2048) == INVALID and r(Gout=8) == INVALID and r(n=-1) == INVALID
+    assert r(n=0) == OK
+    assert r(codes=None) == INVALID and r(oc=None) == INVALID
+    bad = (ctypes.c_void_p * N)(*([BASE] + [None] * (N - 1)))
+    assert r(codes=bad) == INVALID
+    mis = (ctypes.c_void_p * N)(*[BASE + i * (1 << 20) + (8 if i == 2 else 0) for i in range(N)])
+    assert r(codes=mis) == MISALIGNED
+    assert r(sm=sm + 4) == MISALIGNED
+    assert r(oc=BASE + 64) == ALIAS  # output codes on top of shard 0
+    assert r(sm=BASE + (1 << 28) + 16) == ALIAS  # sum on top of shard 0's scales
+    assert r(os=oc + 16) == ALIAS
+
+
+def test_fp8_accumulate_argument_errors(L):
+    c, s, g = BASE, BASE + (1 << 24), BASE + (1 << 26)
+    assert L.zq_fp8_accumulate(c, s, g, 5, 4096, 128, None) == UNSUPPORTED
+    assert L.zq_fp8_accumulate(c, s, g, zq.BF16, 4096, 100, None) == INVALID
+    assert L.zq_fp8_accumulate(c, s, g, zq.BF16, -1, 128, None) == INVALID
+    assert L.zq_fp8_accumulate(None, s, g, zq.BF16, 4096, 128, None) == INVALID
+    assert L.zq_fp8_accumulate(c, s, g + 4, zq.BF16, 4096, 128, None) == MISALIGNED
+    assert L.zq_fp8_accumulate(c, s, c + 1024, zq.BF16, 4096, 128, None) == ALIAS
+    assert L.zq_fp8_accumulate(c, c + 2048, g, zq.BF16, 4096, 128, None) == ALIAS
+    assert L.zq_fp8_accumulate(c, s, g, zq.BF16, 0, 128, None) == OK
