@@ -129,10 +129,14 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 class Launch:
-    __slots__ = ("label", "family", "nbytes", "fn")
+    """One timed unit: `fn` enqueues `kernels` launches of one kernel family
+    that move `nbytes` algorithmic bytes in total."""
 
-    def __init__(self, label, family, nbytes, fn):
+    __slots__ = ("label", "family", "nbytes", "fn", "kernels")
+
+    def __init__(self, label, family, nbytes, fn, kernels=1):
         self.label, self.family, self.nbytes, self.fn = label, family, nbytes, fn
+        self.kernels = kernels
 
 
 def _dev_bf16(bits: np.ndarray):
@@ -249,7 +253,426 @@ class GMSweep:
         return run, nbytes, desc
 
 
-WORKLOADS = {"gm_sweep": GMSweep}
+class QwzFP16:
+    """1,048,576 fp16 weights ~ N(0, 0.02) with 0.1% x50 outliers (seed 0);
+    int8 G=256 quantize and dequantize -> fp32. One call moves 3.2 MB and
+    takes microseconds, so a step replays CUDA graphs of 512 calls on 512
+    distinct tensors (1.6-2.7 GB per graph, far beyond L2); the single-call
+    latency is reported beside it."""
+
+    name = "qwz_fp16"
+    copies = 512
+    n = 1 << 20
+    G = 256
+
+    def __init__(self):
+        from blockwise_quantized_zero_gb300 import inputs
+
+        self.host = inputs.weights_fp16_outliers(self.n)
+
+    def config(self):
+        return {"workload": "qwz_fp16: one fp16 tensor of 1,048,576 elements N(0,0.02) with 0.1% "
+                            "outliers x50 (seed 0), int8 G=256 quantize + dequantize->fp32; "
+                            "timed as CUDA graphs of 512 calls on 512 distinct copies",
+                "elements": self.n, "batched_copies": self.copies,
+                "l2": "no flush: 512 distinct buffers per graph (1.6-2.7 GB per replay)",
+                "single_call_us": getattr(self, "single_call_us", None)}
+
+    def setup(self):
+        import torch
+
+        import blockwise_quantized_zero_gb300 as zq
+
+        self.zq = zq
+        src0 = torch.from_numpy(self.host).cuda()
+        self.src = [src0] + [src0.clone() for _ in range(self.copies - 1)]
+        self.codes = [zq.empty_codes(zq.INT8, self.n, "cuda") for _ in range(self.copies)]
+        self.scales = [zq.empty_scales(self.n, self.G, "cuda") for _ in range(self.copies)]
+        self.out = [torch.empty(self.n, dtype=torch.float32, device="cuda") for _ in range(self.copies)]
+        # single-call latency through the C ABI, host launch included
+        for _ in range(20):
+            zq.quantize(self.src[0], zq.INT8, self.G, self.codes[0], self.scales[0])
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(200):
+            zq.quantize(self.src[i % 8], zq.INT8, self.G, self.codes[i % 8], self.scales[i % 8])
+        torch.cuda.synchronize()
+        self.single_call_us = round((time.perf_counter() - t0) / 200 * 1e6, 2)
+        s = torch.cuda.Stream()
+        self.gq, self.gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            for i in range(self.copies):  # warm the launch paths before capture
+                zq.quantize(self.src[i], zq.INT8, self.G, self.codes[i], self.scales[i])
+                zq.dequantize(self.codes[i], self.scales[i], self.n, zq.INT8, self.G, out=self.out[i])
+        torch.cuda.synchronize()
+        with torch.cuda.graph(self.gq, stream=s):
+            for i in range(self.copies):
+                zq.quantize(self.src[i], zq.INT8, self.G, self.codes[i], self.scales[i])
+        with torch.cuda.graph(self.gd, stream=s):
+            for i in range(self.copies):
+                zq.dequantize(self.codes[i], self.scales[i], self.n, zq.INT8, self.G, out=self.out[i])
+        torch.cuda.synchronize()
+
+    def launches(self):
+        n, k = self.n, self.copies
+        pb = packed_bytes(8, n, self.G)
+        return [Launch(f"quantize fp16 int8 G=256 x{k} (graph)", "quantize", k * (2 * n + pb),
+                       self.gq.replay, kernels=k),
+                Launch(f"dequantize int8 G=256 f32 x{k} (graph)", "dequantize", k * (pb + 4 * n),
+                       self.gd.replay, kernels=k)]
+
+    def setup_e2e(self):
+        import torch
+
+        zq, n = self.zq, self.n
+        self.e_copies = 64
+        self.h_src = torch.from_numpy(self.host).pin_memory()
+        self.h_codes = torch.empty(zq.codes_bytes(zq.INT8, n), dtype=torch.uint8).pin_memory()
+        self.h_scales = torch.empty(zq.num_blocks(n, self.G), dtype=torch.float32).pin_memory()
+        self.h_out = torch.empty(n, dtype=torch.float32).pin_memory()
+        pb = packed_bytes(8, n, self.G)
+        return self.e_copies * (2 * n + pb), self.e_copies * (pb + 4 * n)
+
+    def e2e_step(self):
+        zq, n = self.zq, self.n
+        for i in range(self.e_copies):
+            self.src[i].copy_(self.h_src, non_blocking=True)
+            zq.quantize(self.src[i], zq.INT8, self.G, self.codes[i], self.scales[i])
+            self.h_codes.copy_(self.codes[i], non_blocking=True)
+            self.h_scales.copy_(self.scales[i], non_blocking=True)
+            self.codes[i].copy_(self.h_codes, non_blocking=True)
+            self.scales[i].copy_(self.h_scales, non_blocking=True)
+            zq.dequantize(self.codes[i], self.scales[i], n, zq.INT8, self.G, out=self.out[i])
+            self.h_out.copy_(self.out[i], non_blocking=True)
+
+    def e2e_bytes(self):
+        pb = packed_bytes(8, self.n, self.G)
+        return self.e_copies * (2 * self.n + pb + pb + 4 * self.n)
+
+    def oracle_sample(self, sample=None):
+        import oracle as O
+
+        # whole-tensor round trips; `sample` elements are rounded to whole tensors
+        reps = 256 if sample is None else max(1, sample // self.n)
+        x = self.host if sample is None or sample >= self.n else self.host[:max(1024, sample)]
+        m = x.size
+
+        def run():
+            for _ in range(reps):
+                c, s = O.quantize(x, O.INT8, self.G)
+                O.dequantize(c, s, m, O.INT8, self.G, O.F32)
+
+        pb = packed_bytes(8, m, self.G)
+        return run, reps * (2 * m + pb + pb + 4 * m), \
+            f"{reps} quantize + dequantize->fp32 round trips of {m:,} elements of the fp16 tensor, single thread"
+
+
+class QgzReduce:
+    """8 gradient shards of 134,217,728 fp32 ~ Laplace(0, 1e-4) (seed 3,
+    stream = shard), pre-quantized to int4 G=128 (setup, not timed); a step
+    reduces them to int4 G=128 and, separately, to int8 G=256."""
+
+    name = "qgz_reduce"
+    N = 8
+    n = 134217728
+
+    def config(self):
+        return {"workload": "qgz_reduce: 8 simulated peer shards of 134,217,728 fp32 gradients "
+                            "~Laplace(0,1e-4), pre-quantized to int4 G=128; fused dequant -> fp32 "
+                            "sum in shard order -> requant to int4 G=128 and to int8 G=256",
+                "elements": self.n, "shards": self.N,
+                "l2": "no flush: 570 MB of shard input per launch >> 126 MB L2"}
+
+    def setup(self):
+        import torch
+
+        import blockwise_quantized_zero_gb300 as zq
+        from blockwise_quantized_zero_gb300 import inputs
+
+        self.zq = zq
+        self.codes, self.scales, self.host_sample = [], [], []
+        for r in range(self.N):
+            x = inputs.gradient_shard_f32(self.n, shard=r)
+            self.host_sample.append(x[: 1 << 26].copy())
+            c, s = zq.quantize(torch.from_numpy(x).cuda(), zq.INT4, 128)
+            self.codes.append(c)
+            self.scales.append(s)
+            del x
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        self.oc4, self.os4 = zq.empty_codes(zq.INT4, self.n, "cuda"), zq.empty_scales(self.n, 128, "cuda")
+        self.oc8, self.os8 = zq.empty_codes(zq.INT8, self.n, "cuda"), zq.empty_scales(self.n, 256, "cuda")
+
+    def launches(self):
+        zq, n, N = self.zq, self.n, self.N
+        inb = N * packed_bytes(4, n, 128)
+        return [
+            Launch("reduce 8x int4 G=128 -> int4 G=128", "reduce", inb + packed_bytes(4, n, 128),
+                   lambda: zq.reduce_quantized(self.codes, self.scales, n, zq.INT4, 128, zq.INT4, 128,
+                                               self.oc4, self.os4)),
+            Launch("reduce 8x int4 G=128 -> int8 G=256", "reduce", inb + packed_bytes(8, n, 256),
+                   lambda: zq.reduce_quantized(self.codes, self.scales, n, zq.INT4, 128, zq.INT8, 256,
+                                               self.oc8, self.os8)),
+        ]
+
+    def setup_e2e(self):
+        import torch
+
+        zq, n = self.zq, self.n
+        self.h_codes = [c.cpu().pin_memory() for c in self.codes]
+        self.h_scales = [s.cpu().pin_memory() for s in self.scales]
+        self.h_oc = torch.empty(zq.codes_bytes(zq.INT8, n), dtype=torch.uint8).pin_memory()
+        self.h_os = torch.empty(zq.num_blocks(n, 128), dtype=torch.float32).pin_memory()
+        inb = self.N * packed_bytes(4, n, 128)
+        return 2 * inb, packed_bytes(4, n, 128) + packed_bytes(8, n, 256)
+
+    def e2e_step(self):
+        """Shards from host memory, results to host memory, for both reductions."""
+        zq, n = self.zq, self.n
+        for fout, G, oc, os_ in ((zq.INT4, 128, self.oc4, self.os4), (zq.INT8, 256, self.oc8, self.os8)):
+            for r in range(self.N):
+                self.codes[r].copy_(self.h_codes[r], non_blocking=True)
+                self.scales[r].copy_(self.h_scales[r], non_blocking=True)
+            zq.reduce_quantized(self.codes, self.scales, n, zq.INT4, 128, fout, G, oc, os_)
+            self.h_oc[: oc.numel()].copy_(oc, non_blocking=True)
+            self.h_os[: os_.numel()].copy_(os_, non_blocking=True)
+
+    def oracle_sample(self, sample=1 << 26):
+        import oracle as O
+        from blockwise_quantized_zero_gb300 import inputs
+
+        host = getattr(self, "host_sample", None)
+        if host is None or host[0].size < sample:
+            host = [inputs.gradient_shard_f32(sample, shard=r) for r in range(self.N)]
+        sh = [O.quantize(np.ascontiguousarray(x[:sample]), O.INT4, 128) for x in host]
+
+        def run():
+            O.reduce([c for c, _ in sh], [s for _, s in sh], sample, O.INT4, 128, O.INT4, 128)
+            O.reduce([c for c, _ in sh], [s for _, s in sh], sample, O.INT4, 128, O.INT8, 256)
+
+        inb = self.N * packed_bytes(4, sample, 128)
+        nbytes = 2 * inb + packed_bytes(4, sample, 128) + packed_bytes(8, sample, 256)
+        return run, nbytes, (f"first {sample:,} elements of each of the 8 shards, both reductions, "
+                             "single thread")
+
+
+class AgoqFP8:
+    """E4M3 main gradient of 268,435,456 elements, G=128; a step adds 4
+    micro-batch bf16 gradients ~ N(0, 1e-3) (seed 4, stream = micro-batch) in
+    place, then reduces 8 shards of n/8 elements to one E4M3 output with its
+    own scales (the slices of the main gradient stand in for the slice every
+    peer sends after the all-to-all)."""
+
+    name = "agoq_fp8"
+    n = 268435456
+    G = 128
+    steps = 4
+    N = 8
+
+    def config(self):
+        return {"workload": "agoq_fp8: E4M3 main gradient of 268,435,456 elements, fp32 scale per "
+                            "128-block; 4 accumulate steps of bf16 N(0,1e-3) gradients "
+                            "(dequant -> add in fp32 -> requant, in place), then an 8-shard FP8 "
+                            "local reduce of 8 x 33,554,432 elements in fp32 and requant",
+                "elements": self.n, "micro_batches": self.steps, "reduce_shards": self.N,
+                "l2": "no flush: 1.1 GB moved per accumulate launch >> 126 MB L2"}
+
+    def setup(self):
+        import torch
+
+        import blockwise_quantized_zero_gb300 as zq
+        from blockwise_quantized_zero_gb300 import inputs
+
+        self.zq = zq
+        self.mc = torch.zeros(zq.codes_bytes(zq.E4M3, self.n), dtype=torch.uint8, device="cuda")
+        self.ms = torch.zeros(zq.num_blocks(self.n, self.G), dtype=torch.float32, device="cuda")
+        self.grads = []
+        for k in range(self.steps):
+            g = inputs.gradient_bf16(self.n, step=k)
+            if k == 0:
+                self.host_grad0 = g[: 1 << 26].copy()
+            self.grads.append(_dev_bf16(g))
+            del g
+        m = self.n // self.N
+        self.sc = [self.mc[r * m:(r + 1) * m] for r in range(self.N)]
+        self.ss = [self.ms[r * m // self.G:(r + 1) * m // self.G] for r in range(self.N)]
+        self.oc = zq.empty_codes(zq.E4M3, m, "cuda")
+        self.os = zq.empty_scales(m, self.G, "cuda")
+        for g in self.grads:  # the reduce's inputs hold an accumulated gradient from the start
+            zq.fp8_accumulate(self.mc, self.ms, g, self.G)
+        torch.cuda.synchronize()
+
+    def launches(self):
+        zq, n, G = self.zq, self.n, self.G
+        acc_bytes = 2 * packed_bytes(0x48, n, G) + 2 * n
+        m = n // self.N
+        out = [Launch(f"fp8_accumulate e4m3 G=128 step {k}", "fp8_accumulate", acc_bytes,
+                      lambda k=k: zq.fp8_accumulate(self.mc, self.ms, self.grads[k], G))
+               for k in range(self.steps)]
+        out.append(Launch("reduce 8x e4m3 G=128 -> e4m3 G=128", "reduce",
+                          (self.N + 1) * packed_bytes(0x48, m, G),
+                          lambda: zq.reduce_quantized(self.sc, self.ss, m, zq.E4M3, G, zq.E4M3, G,
+                                                      self.oc, self.os)))
+        return out
+
+    def setup_e2e(self):
+        import torch
+
+        self.h_grad = self.grads[0].cpu().pin_memory()
+        self.h_mc = torch.empty(self.mc.numel(), dtype=torch.uint8).pin_memory()
+        self.h_ms = torch.empty(self.ms.numel(), dtype=torch.float32).pin_memory()
+        self.h_oc = torch.empty(self.oc.numel(), dtype=torch.uint8).pin_memory()
+        self.h_os = torch.empty(self.os.numel(), dtype=torch.float32).pin_memory()
+        return (self.steps * 2 * self.n + self.mc.numel() + 4 * self.ms.numel(),
+                self.mc.numel() + 4 * self.ms.numel() + self.oc.numel() + 4 * self.os.numel())
+
+    def e2e_step(self):
+        """Host main gradient in, 4 host micro-batch gradients, host results out."""
+        zq, G = self.zq, self.G
+        self.mc.copy_(self.h_mc, non_blocking=True)
+        self.ms.copy_(self.h_ms, non_blocking=True)
+        for k in range(self.steps):
+            self.grads[k].copy_(self.h_grad, non_blocking=True)
+            zq.fp8_accumulate(self.mc, self.ms, self.grads[k], G)
+        m = self.n // self.N
+        zq.reduce_quantized(self.sc, self.ss, m, zq.E4M3, G, zq.E4M3, G, self.oc, self.os)
+        self.h_mc.copy_(self.mc, non_blocking=True)
+        self.h_ms.copy_(self.ms, non_blocking=True)
+        self.h_oc.copy_(self.oc, non_blocking=True)
+        self.h_os.copy_(self.os, non_blocking=True)
+
+    def oracle_sample(self, sample=1 << 26):
+        import oracle as O
+        from blockwise_quantized_zero_gb300 import inputs
+
+        g = getattr(self, "host_grad0", None)
+        if g is None or g.size < sample:
+            g = inputs.gradient_bf16(sample, step=0)
+        g = np.ascontiguousarray(g[:sample])
+        G = self.G
+
+        def run():
+            c = np.zeros(sample, np.uint8)
+            s = np.zeros(sample // G, np.float32)
+            for _ in range(self.steps):
+                c, s = O.fp8_accumulate(c, s, g, G, grad_dtype=O.BF16)
+            m = sample // self.N
+            O.reduce([c[r * m:(r + 1) * m] for r in range(self.N)],
+                     [s[r * m // G:(r + 1) * m // G] for r in range(self.N)], m, O.E4M3, G, O.E4M3, G)
+
+        acc = self.steps * (2 * packed_bytes(0x48, sample, G) + 2 * sample)
+        red = (self.N + 1) * packed_bytes(0x48, sample // self.N, G)
+        return run, acc + red, (f"{sample:,}-element main gradient: 4 accumulate steps + 8-shard "
+                                "reduce of its slices, single thread")
+
+
+class Llama70B:
+    """One Llama-3-70B decoder layer's bf16 weights (7 matrices, 855,638,016
+    elements, N(0, 0.02), seed 5): int8 G=256 and 6-bit G=32 quantize +
+    dequantize -> bf16, one call per matrix."""
+
+    name = "llama70b"
+    schemes = ((8, 256), (6, 32))
+
+    def config(self):
+        return {"workload": "llama70b: one Llama-3-70B decoder layer in bf16 (q,o 8192x8192; k,v "
+                            "8192x1024; gate,up 8192x28672; down 28672x8192; 855,638,016 elements, "
+                            "N(0,0.02)), quantize + dequantize->bf16 at int8 G=256 and 6-bit G=32",
+                "elements": 855638016,
+                "l2": "no flush: each launch streams a whole matrix (up to 470 MB)"}
+
+    def setup(self):
+        import torch
+
+        import blockwise_quantized_zero_gb300 as zq
+        from blockwise_quantized_zero_gb300 import inputs
+
+        self.zq = zq
+        self.mats = []
+        for name, r, c, bits in inputs.llama70b_layer_bf16():
+            if name == "q":
+                self.host_q = bits.copy()
+            self.mats.append((name, r * c, _dev_bf16(bits)))
+            del bits
+        self.buf = {}
+        for b, G in self.schemes:
+            for name, n, _ in self.mats:
+                self.buf[(b, G, name)] = (zq.empty_codes(b, n, "cuda"), zq.empty_scales(n, G, "cuda"),
+                                          torch.empty(n, dtype=torch.bfloat16, device="cuda"))
+
+    def launches(self):
+        zq = self.zq
+        out = []
+        for b, G in self.schemes:
+            for name, n, x in self.mats:
+                c, s, y = self.buf[(b, G, name)]
+                nb = 2 * n + packed_bytes(b, n, G)
+                out.append(Launch(f"quantize bf16 int{b} G={G} {name}", "quantize", nb,
+                                  lambda x=x, b=b, G=G, c=c, s=s: zq.quantize(x, b, G, c, s)))
+            for name, n, x in self.mats:
+                c, s, y = self.buf[(b, G, name)]
+                nb = 2 * n + packed_bytes(b, n, G)
+                out.append(Launch(f"dequantize int{b} G={G} bf16 {name}", "dequantize", nb,
+                                  lambda n=n, b=b, G=G, c=c, s=s, y=y: zq.dequantize(c, s, n, b, G, out=y)))
+        return out
+
+    def setup_e2e(self):
+        import torch
+
+        name, n, x = self.mats[4]  # gate, 8192 x 28672
+        self.e_name, self.e_n = name, n
+        self.h_x = x.cpu().pin_memory()
+        self.h_c = torch.empty(n, dtype=torch.uint8).pin_memory()
+        self.h_s = torch.empty(n // 32, dtype=torch.float32).pin_memory()
+        self.h_y = torch.empty(n, dtype=torch.bfloat16).pin_memory()
+        h2d = d2h = 0
+        for b, G in self.schemes:
+            pb = packed_bytes(b, n, G)
+            h2d += 2 * n + pb
+            d2h += pb + 2 * n
+        return h2d, d2h
+
+    def e2e_step(self):
+        """The gate matrix from host memory through both schemes, results to host."""
+        zq, n = self.zq, self.e_n
+        x = self.mats[4][2]
+        for b, G in self.schemes:
+            c, s, y = self.buf[(b, G, self.e_name)]
+            x.copy_(self.h_x, non_blocking=True)
+            zq.quantize(x, b, G, c, s)
+            self.h_c[: c.numel()].copy_(c, non_blocking=True)
+            self.h_s[: s.numel()].copy_(s, non_blocking=True)
+            c.copy_(self.h_c[: c.numel()], non_blocking=True)
+            s.copy_(self.h_s[: s.numel()], non_blocking=True)
+            zq.dequantize(c, s, n, b, G, out=y)
+            self.h_y.copy_(y, non_blocking=True)
+
+    def e2e_bytes(self):
+        n = self.e_n
+        return sum(2 * (2 * n + packed_bytes(b, n, G)) for b, G in self.schemes)
+
+    def oracle_sample(self, sample=1 << 26):
+        import oracle as O
+        from blockwise_quantized_zero_gb300 import inputs
+
+        x = getattr(self, "host_q", None)
+        if x is None or x.size < sample:
+            x = next(inputs.llama70b_layer_bf16(scale_rows=4))[3]
+        sample = min(sample, x.size)
+        x = np.ascontiguousarray(x[:sample])
+
+        def run():
+            for b, G in self.schemes:
+                c, s = O.quantize(x, b, G, dtype=O.BF16)
+                O.dequantize(c, s, sample, b, G, O.BF16)
+
+        nbytes = sum(2 * (2 * sample + packed_bytes(b, sample, G)) for b, G in self.schemes)
+        return run, nbytes, (f"first {sample:,} elements of the q projection, int8 G=256 and 6-bit "
+                             "G=32 round trips, single thread")
+
+
+WORKLOADS = {"gm_sweep": GMSweep, "qwz_fp16": QwzFP16, "qgz_reduce": QgzReduce,
+             "agoq_fp8": AgoqFP8, "llama70b": Llama70B}
 
 
 # ---------------------------------------------------------------------------
@@ -310,11 +733,28 @@ def aggregate(per_rank_bytes: float, elapsed_s: list[float], world: int) -> tupl
 # arms
 # ---------------------------------------------------------------------------
 
+REFERENCE_BUDGET_S = 120.0  # whole reference run (warm-up + timed steps)
+
+
+def reference_sample(wl, steps: int, warmup: int) -> int:
+    """Sample size per step so that (steps + warmup) steps of the oracle take
+    about REFERENCE_BUDGET_S, from a calibration run on a small sample."""
+    probe = 1 << 16
+    run, _, _ = wl.oracle_sample(probe)
+    t0 = time.perf_counter()
+    run()
+    per_elem = (time.perf_counter() - t0) / probe
+    target = REFERENCE_BUDGET_S / max(1, steps + warmup)
+    n = int(target / max(per_elem, 1e-12))
+    return max(1 << 14, min(1 << 26, (n // 1024) * 1024))
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
     wl = WORKLOADS[args.workload]()
-    run, nbytes, desc = wl.oracle_sample(args.oracle_sample)
+    sample = args.oracle_sample if args.oracle_sample else reference_sample(wl, args.steps, args.warmup)
+    run, nbytes, desc = wl.oracle_sample(sample)
     for _ in range(args.warmup):
         run()
     t0 = time.perf_counter()
@@ -333,8 +773,12 @@ def run_reference(args, rank, world):
     return line
 
 
+def _oracle_sample(wl, sample):
+    return wl.oracle_sample() if sample is None else wl.oracle_sample(sample)
+
+
 def time_cpu_baseline(wl, sample):
-    run, nbytes, desc = wl.oracle_sample(sample)
+    run, nbytes, desc = _oracle_sample(wl, sample)
     t0 = time.perf_counter()
     run()
     dt = time.perf_counter() - t0
@@ -397,11 +841,14 @@ def run_gpu(args, rank, world, local):
     dominant = max(fam, key=lambda k: fam[k][0])
     peak, peak_src = measured_peak()
     ms_sum, nbytes, count = fam[dominant]
+    count = sum(l.kernels for l in launches if l.family == dominant) * args.steps
     achieved = nbytes / (ms_sum / 1e3) / 1e9
     traffic = lookup_traffic(dominant)
+    kpl = {l.label: l.kernels for l in launches}
     kernels = {k: {"gbs": round(v[1] / (v[0] / 1e3) / 1e9, 1),
                    "frac": round(v[1] / (v[0] / 1e3) / 1e9 / peak, 3),
-                   "us_per_launch": round(v[0] / v[2] * 1e3, 2), "launches": v[2]}
+                   "us_per_launch": round(v[0] / (v[2] * kpl[k]) * 1e3, 2),
+                   "launches": v[2] * kpl[k]}
                for k, v in per_label.items()}
 
     # end to end through the C ABI with host buffers
@@ -417,7 +864,8 @@ def run_gpu(args, rank, world, local):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
-    e2e_value = world * step_bytes * e2e_steps / e2e_t / 1e9
+    e2e_bytes = wl.e2e_bytes() if hasattr(wl, "e2e_bytes") else step_bytes
+    e2e_value = world * e2e_bytes * e2e_steps / e2e_t / 1e9
 
     cpu = time_cpu_baseline(wl, args.oracle_sample) if (rank == 0 and world == 1 and not args.no_cpu) else None
     if rank != 0:
@@ -438,7 +886,7 @@ def run_gpu(args, rank, world, local):
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-            "gpu_launches": len(launches) * args.steps,
+            "gpu_launches": sum(l.kernels for l in launches) * args.steps,
             "clocks": clocks.summary()}
     return line
 
@@ -475,7 +923,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["zq", "reference"], default="zq")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gm_sweep")
-    ap.add_argument("--oracle-sample", type=int, default=1 << 24)
+    ap.add_argument("--oracle-sample", type=int, default=None,
+                    help="elements in the CPU-oracle sample (default: the workload's own)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "zq":

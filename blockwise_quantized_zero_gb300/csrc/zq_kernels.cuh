@@ -390,55 +390,86 @@ __device__ __noinline__ void reduce_tail(const ReduceArgs &a, int64_t e0, int la
   }
 }
 
+// Shard codes and scales of one batch of shards for one tile (4 shards of
+// codes up to 4 bits, 2 of wider codes, to bound the registers in flight).
+template <int FIN> constexpr int kBatchOf = (Fmt<FIN>::kBits <= 4) ? 4 : 2;
+template <int FIN> struct ShardBatch {
+  uint32_t w[kBatchOf<FIN>][kU][Fmt<FIN>::kWords16];
+  float s[kBatchOf<FIN>][kU];
+};
+
+template <int FIN>
+__device__ __forceinline__ void load_batch(const ReduceArgs &a, int64_t e0, int r0, int lane,
+                                           ShardBatch<FIN> &b) {
+  constexpr int BIN = Fmt<FIN>::kBits, kBatch = kBatchOf<FIN>;
+#pragma unroll
+  for (int k = 0; k < kBatch; ++k) {
+    const int r = r0 + k < a.nshards ? r0 + k : a.nshards - 1;  // past the end: any valid shard
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const int64_t e = e0 + j * kRun + lane * kVec;
+      load_codes16<BIN>(a.codes[r] + e * BIN / 8, b.w[k][j]);
+      b.s[k][j] = ld_nc_f32(a.scales[r] + (e >> a.log2Gin));
+    }
+  }
+}
+
+template <int FIN>
+__device__ __forceinline__ void add_batch(const ReduceArgs &a, int r0, const ShardBatch<FIN> &b,
+                                          float (&acc)[kU][kVec]) {
+  constexpr int kBatch = kBatchOf<FIN>;
+#pragma unroll
+  for (int k = 0; k < kBatch; ++k) {
+    if (r0 + k < a.nshards) {  // shard order is the summation order
+#pragma unroll
+      for (int j = 0; j < kU; ++j) accumulate16<FIN>(acc[j], b.w[k][j], b.s[k][j]);
+    }
+  }
+}
+
+// Software pipeline over (tile, shard batch) units: while one batch is added,
+// the loads of the next unit (the next batch of this tile, or the first batch
+// of the warp's next tile) are in flight. Two register buffers are used in
+// turn, so nothing is copied.
 template <int FIN, int FOUT>
-__global__ void __launch_bounds__(kThreads) reduce_kernel(const __grid_constant__ ReduceArgs a) {
-  constexpr int BIN = Fmt<FIN>::kBits, WIN = Fmt<FIN>::kWords16;
-  constexpr int kBatch = 4;  // shards whose loads are in flight together
+__global__ void __launch_bounds__(kThreads, 2) reduce_kernel(const __grid_constant__ ReduceArgs a) {
+  constexpr int kBatch = kBatchOf<FIN>;
   const WarpCursor c;
   const int64_t nfull = a.n / kTile;
-  for (int64_t t = c.warp; t < nfull; t += c.nwarps) {
-    const int64_t e0 = t * kTile;
-    float acc[kU][kVec];
+  const int nb = (a.nshards + kBatch - 1) / kBatch;  // batches per tile
+  const int64_t my_tiles = c.warp < nfull ? (nfull - 1 - c.warp) / c.nwarps + 1 : 0;
+  const int64_t units = my_tiles * nb;
+  ShardBatch<FIN> buf[2];
+  float acc[kU][kVec];
+  auto unit_tile = [&](int64_t u) { return (c.warp + (u / nb) * c.nwarps) * kTile; };
+  auto unit_batch = [&](int64_t u) { return int(u % nb) * kBatch; };
+  if (units > 0) load_batch<FIN>(a, unit_tile(0), 0, c.lane, buf[0]);
+  for (int64_t u = 0; u < units; u += 2) {
 #pragma unroll
-    for (int j = 0; j < kU; ++j)
+    for (int h = 0; h < 2; ++h) {  // h: the buffer that holds unit u + h
+      const int64_t uu = u + h;
+      if (uu < units) {
+        if (uu + 1 < units)
+          load_batch<FIN>(a, unit_tile(uu + 1), unit_batch(uu + 1), c.lane, buf[h ^ 1]);
+        const int r0 = unit_batch(uu);
+        if (r0 == 0) {
 #pragma unroll
-      for (int v = 0; v < kVec; ++v) acc[j][v] = 0.0f;
-
-    int r = 0;
-    for (; r + kBatch <= a.nshards; r += kBatch) {
-      uint32_t w[kBatch][kU][WIN];
-      float s[kBatch][kU];
+          for (int j = 0; j < kU; ++j)
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k)
-#pragma unroll
-        for (int j = 0; j < kU; ++j) {
-          const int64_t e = e0 + j * kRun + c.lane * kVec;
-          load_codes16<BIN>(a.codes[r + k] + e * BIN / 8, w[k][j]);
-          s[k][j] = ld_nc_f32(a.scales[r + k] + (e >> a.log2Gin));
+            for (int v = 0; v < kVec; ++v) acc[j][v] = 0.0f;
         }
+        add_batch<FIN>(a, r0, buf[h], acc);
+        if (r0 + kBatch >= a.nshards) {  // last batch of the tile
+          const int64_t e0 = unit_tile(uu);
+          if (a.sum_out) {
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k)
-#pragma unroll
-        for (int j = 0; j < kU; ++j) accumulate16<FIN>(acc[j], w[k][j], s[k][j]);
-    }
-    for (; r < a.nshards; ++r) {
-      uint32_t w[kU][WIN];
-      float s[kU];
-#pragma unroll
-      for (int j = 0; j < kU; ++j) {
-        const int64_t e = e0 + j * kRun + c.lane * kVec;
-        load_codes16<BIN>(a.codes[r] + e * BIN / 8, w[j]);
-        s[j] = ld_nc_f32(a.scales[r] + (e >> a.log2Gin));
+            for (int j = 0; j < kU; ++j)
+              store16<DT_F32>(a.sum_out, e0 + j * kRun + c.lane * kVec, acc[j], a.wide != 0);
+          }
+          requant_tile<FOUT>(a, acc, e0, c.lane);
+        }
       }
-#pragma unroll
-      for (int j = 0; j < kU; ++j) accumulate16<FIN>(acc[j], w[j], s[j]);
     }
-    if (a.sum_out) {
-#pragma unroll
-      for (int j = 0; j < kU; ++j)
-        store16<DT_F32>(a.sum_out, e0 + j * kRun + c.lane * kVec, acc[j], a.wide != 0);
-    }
-    requant_tile<FOUT>(a, acc, e0, c.lane);
   }
   if (c.owns_tail(a.n)) reduce_tail<FIN, FOUT>(a, nfull * kTile, c.lane);
 }
