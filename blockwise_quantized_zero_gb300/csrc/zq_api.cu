@@ -231,6 +231,7 @@ zq_status zq_reduce_quantized(const void *const *codes, const float *const *scal
   a.log2Gin = log2_block(G_in);
   a.log2Gout = log2_block(G_out);
   a.wide = (!sum_out || aligned32(sum_out)) ? 1 : 0;
+  a.one = 1.0f;
   return from_cuda(launch_reduce(a, format_in, format_out, as_stream(stream)));
 }
 

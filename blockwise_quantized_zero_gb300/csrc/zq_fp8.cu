@@ -8,7 +8,7 @@ static cudaError_t go_a(void *codes, float *scales, const void *grad, int64_t n,
                         bool wide) {
   constexpr auto K = fp8_accumulate_kernel<DT, G>;
   K<<<grid_for<K>(n), kThreads, 0, st>>>(static_cast<uint8_t *>(codes), scales, grad, n,
-                                          wide ? 1 : 0);
+                                          wide ? 1 : 0, 1.0f);
   return cudaGetLastError();
 }
 

@@ -305,50 +305,77 @@ struct ReduceArgs {
   int log2Gin;
   int log2Gout;
   int wide;
+  float one;  // 1.0f, passed at run time (see accumulate16)
 };
 
-// Add shard r's 16 dequantized values into acc (one binary32 add each).
-// The adds are scalar add.rn.f32 on purpose: ptxas contracts a packed
-// mul.rn.f32x2 feeding a packed add.rn.f32x2 into a fused multiply-add (even
-// with the explicit .rn and -fmad=false), which would skip the rounding of the
-// product that the definition requires; scalar add.rn.f32 is never contracted.
+// Add shard r's 16 dequantized values into acc: acc = fl(acc + fl(q * s)).
+// ptxas contracts a packed mul.rn.f32x2 feeding a packed add.rn.f32x2 into a
+// fused multiply-add (even with the explicit .rn and -fmad=false), which
+// would skip the rounding of the product. The add is therefore written as a
+// packed fma of the rounded product with `one`, a 1.0f that arrives at run
+// time: fl(d * 1 + acc) = fl(d + acc) exactly, and since ptxas cannot know
+// that `one` is 1, it can neither drop the multiply nor fold the product in.
 template <int FIN>
 __device__ __forceinline__ void accumulate16(float (&acc)[kVec],
-                                             const uint32_t (&w)[Fmt<FIN>::kWords16], float s) {
+                                             const uint32_t (&w)[Fmt<FIN>::kWords16], float s,
+                                             float one) {
   float d[kVec];
   dequant16<FIN>(w, s, d);
 #pragma unroll
-  for (int v = 0; v < kVec; ++v) acc[v] = __fadd_rn(acc[v], d[v]);
+  for (int v = 0; v < kVec; v += 2)
+    fma2(acc[v], acc[v + 1], d[v], d[v + 1], one, one, acc[v], acc[v + 1]);
 }
 
-template <int FOUT>
-__device__ __forceinline__ void requant_tile(const ReduceArgs &a, float (&acc)[kU][kVec],
+// Requantize the sums of one tile of KU runs (KU*512 elements) with block
+// size 2^log2Gout (run time). As in quantize: the block absmax is a shuffle
+// tree over the G/16 lanes of a block; lane l then computes the scale (IEEE
+// division) and its reciprocal of block l of the tile, stores it, and the
+// lanes of each block fetch them back with a shuffle.
+template <int FOUT, int KU>
+__device__ __forceinline__ void requant_tile(const ReduceArgs &a, float (&acc)[KU][kVec],
                                              int64_t e0, int lane) {
   constexpr int B = Fmt<FOUT>::kBits, W = Fmt<FOUT>::kWords16;
-  const int Gout = 1 << a.log2Gout;
-  float s[kU], r[kU];
-  if (Gout <= kRun) {
-    const int L = Gout / kVec;
+  const int lg = a.log2Gout;                 // 5 .. 10, and G <= KU * 512
+  float m[KU], s[KU], r[KU];
 #pragma unroll
-    for (int j = 0; j < kU; ++j) {
-      s[j] = block_scale<FOUT>(group_max_rt(absmax16(acc[j]), L));
-      r[j] = safe_rcp(s[j]);
-      if ((lane & (L - 1)) == 0) a.out_scales[(e0 + j * kRun + lane * kVec) >> a.log2Gout] = s[j];
+  for (int j = 0; j < KU; ++j) m[j] = absmax16(acc[j]);
+  if (lg - 4 <= 5) {                         // a block lies within one run
+    const int L = 1 << (lg - 4);             // lanes per block
+#pragma unroll
+    for (int j = 0; j < KU; ++j) m[j] = group_max_rt(m[j], L);
+    const int per_run = 32 >> (lg - 4);      // blocks per run
+    const int src = (lane & (per_run - 1)) << (lg - 4);
+    float mb = __shfl_sync(kFull, m[0], src);
+    if constexpr (KU == 2) {
+      const float m1 = __shfl_sync(kFull, m[1], src);
+      mb = (lane < per_run) ? mb : m1;
     }
-  } else {
-    const float m = warp_max(fmaxf(absmax16(acc[0]), absmax16(acc[1])));
-    s[0] = s[1] = block_scale<FOUT>(m);
-    r[0] = r[1] = safe_rcp(s[0]);
-    if (lane == 0) a.out_scales[e0 >> a.log2Gout] = s[0];
-  }
-  uint32_t w[kU][W];
+    const float sb = block_scale<FOUT>(mb), rb = safe_rcp(sb);
+    if (lane < per_run * KU) a.out_scales[(e0 >> lg) + lane] = sb;
 #pragma unroll
-  for (int j = 0; j < kU; ++j) {
+    for (int j = 0; j < KU; ++j) {
+      const int owner = j * per_run + (lane >> (lg - 4));
+      s[j] = __shfl_sync(kFull, sb, owner);
+      r[j] = __shfl_sync(kFull, rb, owner);
+    }
+  } else {                                   // G = 1024 = the whole two-run tile
+    const float mt = warp_max(KU == 2 ? fmaxf(m[0], m[KU - 1]) : m[0]);
+    const float sb = block_scale<FOUT>(mt), rb = safe_rcp(sb);
+#pragma unroll
+    for (int j = 0; j < KU; ++j) {
+      s[j] = sb;
+      r[j] = rb;
+    }
+    if (lane == 0) a.out_scales[e0 >> lg] = sb;
+  }
+  uint32_t w[KU][W];
+#pragma unroll
+  for (int j = 0; j < KU; ++j) {
     const uint32_t flagged = quant16_try_fast<FOUT>(acc[j], s[j], r[j], w[j]);
     if (flagged) quant16_fix<FOUT>(acc[j], s[j], r[j], flagged, w[j]);
   }
 #pragma unroll
-  for (int j = 0; j < kU; ++j)
+  for (int j = 0; j < KU; ++j)
     store_codes16<B>(a.out_codes + (e0 + j * kRun + lane * kVec) * B / 8, w[j]);
 }
 
@@ -393,85 +420,109 @@ __device__ __noinline__ void reduce_tail(const ReduceArgs &a, int64_t e0, int la
 // Shard codes and scales of one batch of shards for one tile (4 shards of
 // codes up to 4 bits, 2 of wider codes, to bound the registers in flight).
 template <int FIN> constexpr int kBatchOf = (Fmt<FIN>::kBits <= 4) ? 4 : 2;
-template <int FIN> struct ShardBatch {
-  uint32_t w[kBatchOf<FIN>][kU][Fmt<FIN>::kWords16];
-  float s[kBatchOf<FIN>][kU];
+template <int FIN, int KU> struct ShardBatch {
+  uint32_t w[kBatchOf<FIN>][KU][Fmt<FIN>::kWords16];
+  float s[kBatchOf<FIN>][KU];
 };
 
-template <int FIN>
+template <int FIN, int KU>
 __device__ __forceinline__ void load_batch(const ReduceArgs &a, int64_t e0, int r0, int lane,
-                                           ShardBatch<FIN> &b) {
+                                           ShardBatch<FIN, KU> &b) {
   constexpr int BIN = Fmt<FIN>::kBits, kBatch = kBatchOf<FIN>;
+  int64_t coff[KU], soff[KU];
+#pragma unroll
+  for (int j = 0; j < KU; ++j) {
+    const int64_t e = e0 + j * kRun + lane * kVec;
+    coff[j] = e * BIN / 8;
+    soff[j] = e >> a.log2Gin;
+  }
 #pragma unroll
   for (int k = 0; k < kBatch; ++k) {
     const int r = r0 + k < a.nshards ? r0 + k : a.nshards - 1;  // past the end: any valid shard
+    const uint8_t *cr = a.codes[r];
+    const float *sr = a.scales[r];
 #pragma unroll
-    for (int j = 0; j < kU; ++j) {
-      const int64_t e = e0 + j * kRun + lane * kVec;
-      load_codes16<BIN>(a.codes[r] + e * BIN / 8, b.w[k][j]);
-      b.s[k][j] = ld_nc_f32(a.scales[r] + (e >> a.log2Gin));
+    for (int j = 0; j < KU; ++j) {
+      load_codes16<BIN>(cr + coff[j], b.w[k][j]);
+      b.s[k][j] = ld_nc_f32(sr + soff[j]);
     }
   }
 }
 
-template <int FIN>
-__device__ __forceinline__ void add_batch(const ReduceArgs &a, int r0, const ShardBatch<FIN> &b,
-                                          float (&acc)[kU][kVec]) {
+template <int FIN, int KU>
+__device__ __forceinline__ void add_batch(const ReduceArgs &a, int r0,
+                                          const ShardBatch<FIN, KU> &b, float (&acc)[KU][kVec]) {
   constexpr int kBatch = kBatchOf<FIN>;
 #pragma unroll
   for (int k = 0; k < kBatch; ++k) {
     if (r0 + k < a.nshards) {  // shard order is the summation order
 #pragma unroll
-      for (int j = 0; j < kU; ++j) accumulate16<FIN>(acc[j], b.w[k][j], b.s[k][j]);
+      for (int j = 0; j < KU; ++j) accumulate16<FIN>(acc[j], b.w[k][j], b.s[k][j], a.one);
     }
   }
 }
 
-// Software pipeline over (tile, shard batch) units: while one batch is added,
-// the loads of the next unit (the next batch of this tile, or the first batch
-// of the warp's next tile) are in flight. Two register buffers are used in
-// turn, so nothing is copied.
-template <int FIN, int FOUT>
-__global__ void __launch_bounds__(kThreads, 2) reduce_kernel(const __grid_constant__ ReduceArgs a) {
+// Tiles of KU runs (KU * 512 elements; the launcher uses KU = 2, which
+// serves every G_out: measured faster than KU = 1, whose smaller register
+// buffers allow 3 CTAs per SM but double the per-unit overhead). Software
+// pipeline over (tile, shard batch) units:
+// while one batch is added, the loads of the next unit (the next batch of
+// this tile, or the first batch of the warp's next tile) are in flight, in the
+// other of two register buffers, so nothing is copied.
+template <int FIN, int FOUT, int KU>
+__global__ void __launch_bounds__(kThreads, KU == 1 ? 3 : 2)
+    reduce_kernel(const __grid_constant__ ReduceArgs a) {
   constexpr int kBatch = kBatchOf<FIN>;
+  constexpr int TILE = KU * kRun;
   const WarpCursor c;
-  const int64_t nfull = a.n / kTile;
-  const int nb = (a.nshards + kBatch - 1) / kBatch;  // batches per tile
-  const int64_t my_tiles = c.warp < nfull ? (nfull - 1 - c.warp) / c.nwarps + 1 : 0;
-  const int64_t units = my_tiles * nb;
-  ShardBatch<FIN> buf[2];
-  float acc[kU][kVec];
-  auto unit_tile = [&](int64_t u) { return (c.warp + (u / nb) * c.nwarps) * kTile; };
-  auto unit_batch = [&](int64_t u) { return int(u % nb) * kBatch; };
-  if (units > 0) load_batch<FIN>(a, unit_tile(0), 0, c.lane, buf[0]);
-  for (int64_t u = 0; u < units; u += 2) {
+  const int64_t nfull = a.n / TILE;
+  const int64_t stride = c.nwarps * TILE;
+  const int64_t end = nfull * TILE;
+  ShardBatch<FIN, KU> buf[2];
+  float acc[KU][kVec];
+  // cursors of the unit being added (e0, r0) and of the unit being loaded
+  int64_t e0 = c.warp * TILE, le0 = e0;
+  int r0 = 0, lr0 = 0;
+  auto advance = [&](int64_t &e, int &r) {
+    r += kBatch;
+    if (r >= a.nshards) {
+      r = 0;
+      e += stride;
+    }
+  };
+  if (le0 < end) {
+    load_batch<FIN, KU>(a, le0, lr0, c.lane, buf[0]);
+    advance(le0, lr0);
+  }
+  while (e0 < end) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {  // h: the buffer that holds unit u + h
-      const int64_t uu = u + h;
-      if (uu < units) {
-        if (uu + 1 < units)
-          load_batch<FIN>(a, unit_tile(uu + 1), unit_batch(uu + 1), c.lane, buf[h ^ 1]);
-        const int r0 = unit_batch(uu);
+    for (int h = 0; h < 2; ++h) {  // h: the buffer that holds the unit (e0, r0)
+      if (e0 < end) {
+        if (le0 < end) {
+          load_batch<FIN, KU>(a, le0, lr0, c.lane, buf[h ^ 1]);
+          advance(le0, lr0);
+        }
         if (r0 == 0) {
 #pragma unroll
-          for (int j = 0; j < kU; ++j)
+          for (int j = 0; j < KU; ++j)
 #pragma unroll
             for (int v = 0; v < kVec; ++v) acc[j][v] = 0.0f;
         }
-        add_batch<FIN>(a, r0, buf[h], acc);
+        add_batch<FIN, KU>(a, r0, buf[h], acc);
         if (r0 + kBatch >= a.nshards) {  // last batch of the tile
-          const int64_t e0 = unit_tile(uu);
           if (a.sum_out) {
 #pragma unroll
-            for (int j = 0; j < kU; ++j)
+            for (int j = 0; j < KU; ++j)
               store16<DT_F32>(a.sum_out, e0 + j * kRun + c.lane * kVec, acc[j], a.wide != 0);
           }
-          requant_tile<FOUT>(a, acc, e0, c.lane);
+          requant_tile<FOUT, KU>(a, acc, e0, c.lane);
         }
+        advance(e0, r0);
       }
     }
   }
-  if (c.owns_tail(a.n)) reduce_tail<FIN, FOUT>(a, nfull * kTile, c.lane);
+  // the partial last tile goes to the warp that would take tile n / TILE
+  if ((a.n % TILE) != 0 && c.warp == nfull % c.nwarps) reduce_tail<FIN, FOUT>(a, end, c.lane);
 }
 
 // ===========================================================================
@@ -483,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 2) reduce_kernel(const __grid_consta
 template <int DT, int G>
 __device__ __forceinline__ void fp8acc_tile(uint8_t *codes, float *scales,
                                             const void *__restrict__ grad, int64_t e0, int lane,
-                                            bool wide) {
+                                            bool wide, float one) {
   float v[kU][kVec];
   uint32_t w[kU][4];
   float sold[kU];
@@ -498,10 +549,10 @@ __device__ __forceinline__ void fp8acc_tile(uint8_t *codes, float *scales,
   for (int j = 0; j < kU; ++j) {
     float d[kVec];
     dequant16<F_E4M3>(w[j], sold[j], d);
-    // scalar adds: see accumulate16 (a packed add after the packed product
-    // would be fused with it)
+    // v = fl(d + g) as a packed fma with the run-time 1.0f (see accumulate16)
 #pragma unroll
-    for (int k = 0; k < kVec; ++k) v[j][k] = __fadd_rn(d[k], v[j][k]);
+    for (int k = 0; k < kVec; k += 2)
+      fma2(v[j][k], v[j][k + 1], d[k], d[k + 1], one, one, v[j][k], v[j][k + 1]);
   }
   float s[kU], r[kU];
   if constexpr (G <= kRun) {
@@ -560,11 +611,11 @@ __device__ __noinline__ void fp8acc_tail(uint8_t *codes, float *scales,
 template <int DT, int G>
 __global__ void __launch_bounds__(kThreads) fp8_accumulate_kernel(uint8_t *codes, float *scales,
                                                                   const void *__restrict__ grad,
-                                                                  int64_t n, int wide) {
+                                                                  int64_t n, int wide, float one) {
   const WarpCursor c;
   const int64_t nfull = n / kTile;
   for (int64_t t = c.warp; t < nfull; t += c.nwarps)
-    fp8acc_tile<DT, G>(codes, scales, grad, t * kTile, c.lane, wide != 0);
+    fp8acc_tile<DT, G>(codes, scales, grad, t * kTile, c.lane, wide != 0, one);
   if (c.owns_tail(n)) fp8acc_tail<DT, G>(codes, scales, grad, nfull * kTile, n, c.lane);
 }
 

@@ -4,10 +4,15 @@
 
 namespace zq {
 
-template <int FIN, int FOUT> static cudaError_t go_r(const ReduceArgs &a, cudaStream_t st) {
-  constexpr auto K = reduce_kernel<FIN, FOUT>;
-  K<<<grid_for<K>(a.n), kThreads, 0, st>>>(a);
+template <int FIN, int FOUT, int KU> static cudaError_t go_r_u(const ReduceArgs &a, cudaStream_t st) {
+  constexpr auto K = reduce_kernel<FIN, FOUT, KU>;
+  // grid_for counts 1024-element tiles; a KU = 1 tile is half of one
+  K<<<grid_for<K>(a.n * (2 / KU)), kThreads, 0, st>>>(a);
   return cudaGetLastError();
+}
+
+template <int FIN, int FOUT> static cudaError_t go_r(const ReduceArgs &a, cudaStream_t st) {
+  return go_r_u<FIN, FOUT, 2>(a, st);
 }
 
 template <int FIN> static cudaError_t go_r_o(const ReduceArgs &a, int fout, cudaStream_t st) {
