@@ -153,11 +153,13 @@ class GMSweep:
     bits = (2, 4, 6, 8)
     blocks = (1024, 512, 256, 128, 64, 32)
 
-    def __init__(self):
+    def __init__(self, pair=None):
         from blockwise_quantized_zero_gb300 import inputs
 
         self.n = self.rows * self.cols
         self.pairs = [(b, G) for b in self.bits for G in self.blocks]
+        if pair is not None:  # one (b, G) pair only, e.g. for a profiler capture
+            self.pairs = [pair]
         self.host = inputs.weight_shard_bf16(self.rows, self.cols)
 
     def config(self):
@@ -165,6 +167,7 @@ class GMSweep:
                             "N(0,0.02)); quantize + dequantize->bf16 for b in {2,4,6,8} x "
                             "G in {1024,512,256,128,64,32}",
                 "elements": self.n, "pairs": len(self.pairs),
+                "pair_subset": None if len(self.pairs) == 24 else [list(p) for p in self.pairs],
                 "l2": "no flush: each of the 48 launches per step reads and writes its own "
                       "buffers (7.7 GB touched per step >> 126 MB L2)"}
 
@@ -749,10 +752,19 @@ def reference_sample(wl, steps: int, warmup: int) -> int:
     return max(1 << 14, min(1 << 26, (n // 1024) * 1024))
 
 
+def make_workload(args):
+    if args.pair:
+        if args.workload != "gm_sweep":
+            raise SystemExit("--pair applies to --workload gm_sweep only")
+        b, G = (int(v) for v in args.pair.split(":"))
+        return GMSweep(pair=(b, G))
+    return WORKLOADS[args.workload]()
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    wl = WORKLOADS[args.workload]()
+    wl = make_workload(args)
     sample = args.oracle_sample if args.oracle_sample else reference_sample(wl, args.steps, args.warmup)
     run, nbytes, desc = wl.oracle_sample(sample)
     for _ in range(args.warmup):
@@ -790,7 +802,7 @@ def run_gpu(args, rank, world, local):
     import torch
 
     torch.cuda.set_device(local)
-    wl = WORKLOADS[args.workload]()
+    wl = make_workload(args)
     wl.setup()
     launches = wl.launches()
     stream = torch.cuda.current_stream()
@@ -926,6 +938,8 @@ def main(argv=None):
     ap.add_argument("--oracle-sample", type=int, default=None,
                     help="elements in the CPU-oracle sample (default: the workload's own)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--pair", default=None,
+                    help="gm_sweep only: run just one (b, G) pair, given as b:G (for profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "zq":
         ap.error("at least 3 warm-up steps")
