@@ -73,59 +73,59 @@ __device__ __forceinline__ void tile_scales(const float (&m)[kU], float (&s)[kU]
 }
 
 // Runs (16 elements of one lane) that the fast path could not decide are not
-// fixed in place, where one flagged lane would hold up its whole warp; their
-// start indices go to a per-warp queue in shared memory, and the warp fixes
-// them 32 at a time, one run per lane, re-reading the source (the scale was
-// already stored). kQueue entries per warp; a flush runs when fewer than 64
-// free slots remain (one tile adds at most 64 runs).
-constexpr int kQueue = 128;
+// fixed in place, where one flagged lane would hold up its whole warp: they go
+// to a per-warp queue in shared memory (start index, block scale and, for
+// 16-bit sources, the run's raw words), and the warp fixes them 32 at a time,
+// one run per lane, as soon as 32 are queued; the last partial batch is fixed
+// when the warp runs out of tiles. A tile adds at most 64 runs to fewer than
+// 32 pending ones, so 96 entries suffice.
+constexpr int kQueue = 96;
 constexpr int kWarps = kThreads / 32;
+template <int DT> constexpr bool kStash = (DT != DT_F32);
 
-// Fix the queued runs q[0 .. count): lane i takes entry base + i, re-reads
-// the source and the stored scale and code words (coherent loads: this warp
-// wrote them), patches the elements that need the exact path, and stores.
+template <int DT> struct FixQueue {
+  int64_t e[kWarps][kQueue];
+  float s[kWarps][kQueue];
+  uint32_t raw[kStash<DT> ? kWarps : 1][kStash<DT> ? kQueue : 1][kRawWords<DT>];
+};
+
+// Fix the queued runs [first, first + count) of warp w: lane i takes entry
+// first + i, recomputes its 16 codes with the exact resolution of the
+// flagged elements, and overwrites the fast-path code words.
 template <int DT, int FMT, int G>
-__device__ __noinline__ void quantize_flush(const int64_t *q, int count,
+__device__ __noinline__ void quantize_flush(FixQueue<DT> &fq, int w, int first, int count,
                                             const void *__restrict__ src,
-                                            uint8_t *__restrict__ codes, const float *scales,
-                                            int lane, bool wide) {
+                                            uint8_t *__restrict__ codes, int lane, bool wide) {
   constexpr int B = Fmt<FMT>::kBits, W = Fmt<FMT>::kWords16;
-  __syncwarp();  // queue entries, scales and fast-path codes of all lanes are visible
+  __syncwarp();  // queue entries and fast-path codes of all lanes are visible
   for (int base = 0; base < count; base += 32) {
     const int i = base + lane;
     if (i < count) {
-      const int64_t e = q[i];
+      const int slot = first + i;
+      const int64_t e = fq.e[w][slot];
+      const float s = fq.s[w][slot];
       uint32_t raw[kRawWords<DT>];
+      if constexpr (kStash<DT>) {
+#pragma unroll
+        for (int k = 0; k < kRawWords<DT>; ++k) raw[k] = fq.raw[w][slot][k];
+      } else {
+        load16_raw<DT>(src, e, raw, wide);
+      }
       float x[kVec];
-      load16_raw<DT>(src, e, raw, wide);
       widen16<DT>(raw, x);
-      const float s = scales[e / G];
       const float r = safe_rcp(s);
       uint8_t *cp = codes + e * B / 8;
-      uint32_t w[W];
+      uint32_t wd[W];
       const bool normal = (FMT == F_E4M3) ? scale_is_normal(s) : (s == 0.0f || scale_is_normal(s));
       if (normal && FMT != F_E4M3) {
-        quant16_fix<FMT>(x, s, r, 1u, w);  // recomputes the run; needs no old words
+        quant16_fix<FMT>(x, s, r, 1u, wd);  // recomputes the run; needs no old words
       } else if (normal) {
-        if constexpr (B == 2) {
-          w[0] = *reinterpret_cast<const uint32_t *>(cp);
-        } else if constexpr (B == 4) {
-          const uint2 v = *reinterpret_cast<const uint2 *>(cp);
-          w[0] = v.x;
-          w[1] = v.y;
-        } else if constexpr (B == 6) {
-          const uint32_t *p = reinterpret_cast<const uint32_t *>(cp);
-          w[0] = p[0];
-          w[1] = p[1];
-          w[2] = p[2];
-        } else {
-          ld_v4(cp, w[0], w[1], w[2], w[3]);
-        }
-        quant16_fix<FMT>(x, s, r, 1u, w);
+        ld_v4(cp, wd[0], wd[1], wd[2], wd[3]);  // E4M3: 16 code bytes
+        quant16_fix<FMT>(x, s, r, 1u, wd);
       } else {
-        quant16_exact<FMT>(x, s, w);
+        quant16_exact<FMT>(x, s, wd);
       }
-      store_codes16<B>(cp, w);
+      store_codes16<B>(cp, wd);
     }
   }
   __syncwarp();
@@ -135,7 +135,7 @@ template <int DT, int FMT, int G>
 __device__ __forceinline__ void quantize_tile(const uint32_t (&raw)[kU][kRawWords<DT>],
                                               uint8_t *__restrict__ codes,
                                               float *__restrict__ scales, int64_t e0, int lane,
-                                              int64_t *q, int &count) {
+                                              FixQueue<DT> &fq, int w, int &count) {
   constexpr int B = Fmt<FMT>::kBits, W = Fmt<FMT>::kWords16;
   float x[kU][kVec];
   float m[kU];
@@ -155,13 +155,21 @@ __device__ __forceinline__ void quantize_tile(const uint32_t (&raw)[kU][kRawWord
 
 #pragma unroll
   for (int j = 0; j < kU; ++j) {
-    uint32_t w[W];
+    uint32_t wd[W];
     const int64_t e = e0 + j * kRun + lane * kVec;
-    const uint32_t flagged = quant16_try_fast<FMT>(x[j], s[j], r[j], w);
-    store_codes16<B>(codes + e * B / 8, w);
+    const uint32_t flagged = quant16_try_fast<FMT>(x[j], s[j], r[j], wd);
+    store_codes16<B>(codes + e * B / 8, wd);
     const unsigned ballot = __ballot_sync(kFull, flagged != 0u);
     if (ballot) {
-      if (flagged) q[count + __popc(ballot & ((1u << lane) - 1u))] = e;
+      if (flagged) {
+        const int slot = count + __popc(ballot & ((1u << lane) - 1u));
+        fq.e[w][slot] = e;
+        fq.s[w][slot] = s[j];
+        if constexpr (kStash<DT>) {
+#pragma unroll
+          for (int k = 0; k < kRawWords<DT>; ++k) fq.raw[w][slot][k] = raw[j][k];
+        }
+      }
       count += __popc(ballot);
     }
   }
@@ -206,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 3) quantize_kernel(const void *__res
   const WarpCursor c;
   const int64_t nfull = n / kTile;
   const bool wd = wide != 0;
-  __shared__ int64_t queue[kWarps][kQueue];
-  int64_t *q = queue[threadIdx.x >> 5];
+  __shared__ FixQueue<DT> fq;
+  const int w = threadIdx.x >> 5;
   int count = 0;  // warp-uniform
   // Software pipeline: the loads of tile t + nwarps are in flight while
   // tile t is quantized.
@@ -229,13 +237,13 @@ __global__ void __launch_bounds__(kThreads, 3) quantize_kernel(const void *__res
       for (int j = 0; j < kU; ++j)
         load16_raw<DT>(src, tn * kTile + j * kRun + c.lane * kVec, raw[j], wd);
     }
-    quantize_tile<DT, FMT, G>(cur, codes, scales, t * kTile, c.lane, q, count);
-    if (count > kQueue - 2 * 32) {
-      quantize_flush<DT, FMT, G>(q, count, src, codes, scales, c.lane, wd);
-      count = 0;
+    quantize_tile<DT, FMT, G>(cur, codes, scales, t * kTile, c.lane, fq, w, count);
+    while (count >= 32) {  // fix full batches right away, newest first
+      count -= 32;
+      quantize_flush<DT, FMT, G>(fq, w, count, 32, src, codes, c.lane, wd);
     }
   }
-  if (count) quantize_flush<DT, FMT, G>(q, count, src, codes, scales, c.lane, wd);
+  if (count) quantize_flush<DT, FMT, G>(fq, w, 0, count, src, codes, c.lane, wd);
   if (c.owns_tail(n)) quantize_tail<DT, FMT, G>(src, codes, scales, nfull * kTile, n, c.lane);
 }
 
