@@ -820,6 +820,11 @@ def run_gpu(args, rank, world, local):
         step()
     torch.cuda.synchronize()
 
+    # Two timed regions of K steps each. The first runs the launches back to
+    # back, as a user's stream does (the kernels use programmatic dependent
+    # launch, which an event recorded between two launches would defeat): it
+    # gives `value`. The second brackets every launch with an event pair: it
+    # gives each kernel's own duration for the roofline.
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in launches] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -828,8 +833,12 @@ def run_gpu(args, rank, world, local):
         torch.cuda.synchronize()
         t_start.record(stream)
         for k in range(args.steps):
-            step(evs[k])
+            step()
         t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        for k in range(args.steps):
+            step(evs[k])
         torch.cuda.synchronize()
         barrier(world)
     elapsed = t_start.elapsed_time(t_end) / 1e3
@@ -899,6 +908,8 @@ def run_gpu(args, rank, world, local):
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": sum(l.kernels for l in launches) * args.steps,
+            "gpu_launches_note": "per timed region; a second region of as many launches, "
+                                 "each bracketed by events, times the kernels one by one",
             "clocks": clocks.summary()}
     return line
 

@@ -34,6 +34,26 @@ template <auto Kernel> unsigned grid_for(int64_t n) {
   return static_cast<unsigned>(ctas < cap ? ctas : cap);
 }
 
+// Launch with programmatic dependent launch allowed: the kernel may be
+// scheduled while the previous kernel on the stream drains; every kernel of
+// this library waits for its predecessor (griddepcontrol.wait) before it
+// touches global memory, so stream order and memory visibility are those of
+// an ordinary launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Launchers (one translation unit each). They return the launch status.
 cudaError_t launch_quantize(const void *src, int dt, int64_t n, int fmt, int64_t G, void *codes,
                             float *scales, cudaStream_t st, bool wide);

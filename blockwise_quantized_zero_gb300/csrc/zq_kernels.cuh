@@ -22,10 +22,19 @@ constexpr int kU = 2;                      // 16-element runs per lane per tile
 constexpr int kTile = 32 * kVec * kU;      // 1024 elements per warp tile
 constexpr int kRun = 32 * kVec;            // 512 elements per warp-wide run
 
+// Programmatic dependent launch: wait until the previous grid on the stream
+// has completed and its writes are visible, then let the next grid be
+// scheduled. Every kernel calls this before its first global memory access.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 struct WarpCursor {
   int lane;
   int64_t warp, nwarps;
   __device__ __forceinline__ WarpCursor() {
+    pdl_enter();
     lane = threadIdx.x & 31;
     warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;

@@ -8,9 +8,8 @@ template <int DT, int FMT, int G>
 static cudaError_t go_q(const void *src, int64_t n, void *codes, float *scales, cudaStream_t st,
                         bool wide) {
   constexpr auto K = quantize_kernel<DT, FMT, G>;
-  K<<<grid_for<K>(n), kThreads, 0, st>>>(src, static_cast<uint8_t *>(codes), scales, n,
-                                          wide ? 1 : 0);
-  return cudaGetLastError();
+  return launch_pdl(K, grid_for<K>(n), st, src, static_cast<uint8_t *>(codes), scales, n,
+                    wide ? 1 : 0);
 }
 
 template <int DT, int FMT>

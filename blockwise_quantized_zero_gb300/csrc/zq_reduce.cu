@@ -7,8 +7,7 @@ namespace zq {
 template <int FIN, int FOUT, int KU> static cudaError_t go_r_u(const ReduceArgs &a, cudaStream_t st) {
   constexpr auto K = reduce_kernel<FIN, FOUT, KU>;
   // grid_for counts 1024-element tiles; a KU = 1 tile is half of one
-  K<<<grid_for<K>(a.n * (2 / KU)), kThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(K, grid_for<K>(a.n * (2 / KU)), st, a);
 }
 
 template <int FIN, int FOUT> static cudaError_t go_r(const ReduceArgs &a, cudaStream_t st) {
