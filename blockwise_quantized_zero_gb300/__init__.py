@@ -62,6 +62,8 @@ def _declare(L):
     L.zq_status_string.restype = ctypes.c_char_p
     L.zq_last_cuda_error.argtypes = []
     L.zq_last_cuda_error.restype = i32
+    L.zq_device_status.argtypes = [vp]
+    L.zq_device_status.restype = i32
     return L
 
 
@@ -189,3 +191,11 @@ def fp8_accumulate(main_codes, main_scales, grad, G: int, stream=None):
                                    dtype_code(grad.dtype), grad.numel(), G,
                                    _stream(grad, stream)), "zq_fp8_accumulate")
     return main_codes, main_scales
+
+
+def device_status(stream=None):
+    """Wait for the stream, then raise ZQError if a kernel's bounded device-side
+    wait ran out since the last check (the library's device error words)."""
+    torch = _torch()
+    st = stream if stream is not None else torch.cuda.current_stream()
+    _check(lib().zq_device_status(ctypes.c_void_p(st.cuda_stream)), "zq_device_status")

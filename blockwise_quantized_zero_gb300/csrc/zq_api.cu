@@ -146,6 +146,16 @@ const char *zq_status_string(int status) {
 
 int zq_last_cuda_error(void) { return g_last_cuda_error; }
 
+zq_status zq_device_status(void *stream) {
+  const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    g_last_cuda_error = static_cast<int>(e);
+    return ZQ_ERR_CUDA;
+  }
+  const unsigned err = zq::take_reduce_device_error();
+  return (err & zq::kDevErrWaitTimeout) ? ZQ_ERR_TIMEOUT : ZQ_OK;
+}
+
 zq_status zq_quantize(const void *src, int src_dtype, int64_t n, int format, int64_t G, void *codes,
                       float *scales, void *stream) {
   if (!bits_of(format) || !elem_bytes(src_dtype)) return ZQ_ERR_UNSUPPORTED;

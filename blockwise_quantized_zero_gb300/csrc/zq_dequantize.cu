@@ -7,7 +7,7 @@ template <int FMT, int DT>
 static cudaError_t go_d(const void *codes, const float *scales, int64_t n, int64_t G, void *dst,
                         cudaStream_t st, bool wide) {
   constexpr auto K = dequantize_kernel<FMT, DT>;
-  return launch_pdl(K, grid_for<K>(n), st, static_cast<const uint8_t *>(codes), scales, dst, n,
+  return launch_pdl(K, grid_for<K>(n), 0, st, static_cast<const uint8_t *>(codes), scales, dst, n,
                     log2_block(G), wide ? 1 : 0);
 }
 

@@ -7,7 +7,7 @@ template <int DT, int G>
 static cudaError_t go_a(void *codes, float *scales, const void *grad, int64_t n, cudaStream_t st,
                         bool wide) {
   constexpr auto K = fp8_accumulate_kernel<DT, G>;
-  return launch_pdl(K, grid_for<K>(n), st, static_cast<uint8_t *>(codes), scales, grad, n,
+  return launch_pdl(K, grid_for<K>(n), 0, st, static_cast<uint8_t *>(codes), scales, grad, n,
                     wide ? 1 : 0, 1.0f);
 }
 

@@ -12,14 +12,22 @@ namespace zq {
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count();
 
-// Resident CTAs per SM for one kernel instantiation (computed once).
-template <auto Kernel> int ctas_per_sm() {
+// Resident CTAs per SM for one kernel instantiation with SMEM bytes of
+// dynamic shared memory (computed once; a kernel that needs more than the
+// default 48 KB is granted it first). 0 if the kernel cannot be made to fit.
+template <auto Kernel, int SMEM = 0, int THREADS = kThreads> int ctas_per_sm() {
   static const int v = [] {
+    if (SMEM > 48 * 1024 &&
+        cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) !=
+            cudaSuccess) {
+      (void)cudaGetLastError();
+      return 0;
+    }
     int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, Kernel, kThreads, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, Kernel, THREADS, SMEM) != cudaSuccess ||
         b < 1) {
       (void)cudaGetLastError();
-      b = 1;
+      b = SMEM > 0 ? 0 : 1;
     }
     return b;
   }();
@@ -27,11 +35,12 @@ template <auto Kernel> int ctas_per_sm() {
 }
 
 // Persistent grid: enough CTAs for every warp tile, at most one wave.
-template <auto Kernel> unsigned grid_for(int64_t n) {
+template <auto Kernel, int SMEM = 0> unsigned grid_for(int64_t n) {
   const int64_t tiles = (n + kTile - 1) / kTile;
   const int64_t ctas = (tiles + kThreads / 32 - 1) / (kThreads / 32);
-  const int64_t cap = int64_t(device_sm_count()) * ctas_per_sm<Kernel>();
-  return static_cast<unsigned>(ctas < cap ? ctas : cap);
+  const int64_t cap = int64_t(device_sm_count()) * ctas_per_sm<Kernel, SMEM>();
+  const int64_t g = ctas < cap ? ctas : cap;
+  return static_cast<unsigned>(g > 0 ? g : 1);
 }
 
 // Launch with programmatic dependent launch allowed: the kernel may be
@@ -40,11 +49,12 @@ template <auto Kernel> unsigned grid_for(int64_t n) {
 // touches global memory, so stream order and memory visibility are those of
 // an ordinary launch.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, cudaStream_t st, Args... args) {
+cudaError_t launch_pdl_threads(void (*kernel)(KArgs...), unsigned grid, unsigned threads,
+                               size_t smem, cudaStream_t st, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -54,12 +64,21 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, cudaStream_t st,
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, size_t smem, cudaStream_t st,
+                       Args... args) {
+  return launch_pdl_threads(kernel, grid, kThreads, smem, st, args...);
+}
+
 // Launchers (one translation unit each). They return the launch status.
 cudaError_t launch_quantize(const void *src, int dt, int64_t n, int fmt, int64_t G, void *codes,
                             float *scales, cudaStream_t st, bool wide);
 cudaError_t launch_dequantize(const void *codes, const float *scales, int64_t n, int fmt,
                               int64_t G, void *dst, int dt, cudaStream_t st, bool wide);
 cudaError_t launch_reduce(const ReduceArgs &a, int fin, int fout, cudaStream_t st);
+// Reads and clears the device error words of the launch units.
+unsigned take_reduce_device_error();
+
 cudaError_t launch_fp8_accumulate(void *codes, float *scales, const void *grad, int dt, int64_t n,
                                   int64_t G, cudaStream_t st, bool wide);
 

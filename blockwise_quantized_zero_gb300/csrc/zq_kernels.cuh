@@ -434,112 +434,196 @@ __device__ __noinline__ void reduce_tail(const ReduceArgs &a, int64_t e0, int la
   }
 }
 
-// Shard codes and scales of one batch of shards for one tile (4 shards of
-// codes up to 4 bits, 2 of wider codes, to bound the registers in flight).
-template <int FIN> constexpr int kBatchOf = (Fmt<FIN>::kBits <= 4) ? 4 : 2;
-template <int FIN, int KU> struct ShardBatch {
-  uint32_t w[kBatchOf<FIN>][KU][Fmt<FIN>::kWords16];
-  float s[kBatchOf<FIN>][KU];
+// Codes of one lane-vector (16 codes, 2*b bytes) from shared memory.
+template <int BITS>
+__device__ __forceinline__ void load_codes16_smem(const uint8_t *p, uint32_t (&w)[BITS / 2]) {
+  if constexpr (BITS == 2) {
+    w[0] = *reinterpret_cast<const uint32_t *>(p);
+  } else if constexpr (BITS == 4) {
+    const uint2 v = *reinterpret_cast<const uint2 *>(p);
+    w[0] = v.x;
+    w[1] = v.y;
+  } else if constexpr (BITS == 6) {  // 12 bytes at a 4-byte aligned offset
+    const uint32_t *q = reinterpret_cast<const uint32_t *>(p);
+    w[0] = q[0];
+    w[1] = q[1];
+    w[2] = q[2];
+  } else {
+    const uint4 v = *reinterpret_cast<const uint4 *>(p);
+    w[0] = v.x;
+    w[1] = v.y;
+    w[2] = v.z;
+    w[3] = v.w;
+  }
+}
+
+// Shared-memory pipeline of the reduce (warp-specialized). A CTA has eight
+// consumer warps and one producer warp. A CTA tile is eight consecutive
+// 1024-element tiles (one per consumer warp); a unit is one CTA tile of
+// kShards consecutive shards. For every shard of a unit the producer brings
+// in the codes of the CTA tile with one bulk copy (and its scales with
+// another when their byte count is a multiple of 16, i.e. always for
+// G_in <= 256 and for whole CTA tiles), into one of kStages stage buffers.
+// Each stage has a "full" barrier (armed by the producer with the byte count)
+// and an "empty" barrier (one arrival per consumer warp once it has read the
+// stage).
+constexpr int kRedConsumers = 8;
+constexpr int kRedThreads = (kRedConsumers + 1) * 32;
+
+template <int FIN> struct RedGeom {
+  static constexpr int kCodeBytes = kTile * Fmt<FIN>::kBits / 8;  // one shard, one tile
+  static constexpr int kShardBytes =                               // codes + room for G_in = 32
+      kRedConsumers * kCodeBytes + kRedConsumers * (kTile / 32) * 4;
+  static constexpr int kShards = (24576 / kShardBytes) > 1 ? 24576 / kShardBytes : 1;
+  static constexpr int kScaleOff = kShards * kRedConsumers * kCodeBytes;
+  static constexpr int kStage = kShards * kShardBytes;
+  static constexpr int kStages = 4;
+  static constexpr int kBarOff = kStages * kStage;
+  static constexpr int kSmem = kBarOff + kStages * 16;  // full + empty barrier per stage
+  static_assert(kCodeBytes % 16 == 0 && kStage % 16 == 0, "bulk copies need 16-byte multiples");
 };
 
-template <int FIN, int KU>
-__device__ __forceinline__ void load_batch(const ReduceArgs &a, int64_t e0, int r0, int lane,
-                                           ShardBatch<FIN, KU> &b) {
-  constexpr int BIN = Fmt<FIN>::kBits, kBatch = kBatchOf<FIN>;
-  int64_t coff[KU], soff[KU];
-#pragma unroll
-  for (int j = 0; j < KU; ++j) {
-    const int64_t e = e0 + j * kRun + lane * kVec;
-    coff[j] = e * BIN / 8;
-    soff[j] = e >> a.log2Gin;
-  }
-#pragma unroll
-  for (int k = 0; k < kBatch; ++k) {
-    const int r = r0 + k < a.nshards ? r0 + k : a.nshards - 1;  // past the end: any valid shard
-    const uint8_t *cr = a.codes[r];
-    const float *sr = a.scales[r];
-#pragma unroll
-    for (int j = 0; j < KU; ++j) {
-      load_codes16<BIN>(cr + coff[j], b.w[k][j]);
-      b.s[k][j] = ld_nc_f32(sr + soff[j]);
-    }
-  }
-}
+// Device error word of this translation unit (read by zq_device_status).
+static __device__ unsigned int g_dev_error = 0;
 
-template <int FIN, int KU>
-__device__ __forceinline__ void add_batch(const ReduceArgs &a, int r0,
-                                          const ShardBatch<FIN, KU> &b, float (&acc)[KU][kVec]) {
-  constexpr int kBatch = kBatchOf<FIN>;
-#pragma unroll
-  for (int k = 0; k < kBatch; ++k) {
-    if (r0 + k < a.nshards) {  // shard order is the summation order
-#pragma unroll
-      for (int j = 0; j < KU; ++j) accumulate16<FIN>(acc[j], b.w[k][j], b.s[k][j], a.one);
-    }
-  }
-}
-
-// Tiles of KU runs (KU * 512 elements; the launcher uses KU = 2, which
-// serves every G_out: measured faster than KU = 1, whose smaller register
-// buffers allow 3 CTAs per SM but double the per-unit overhead). Software
-// pipeline over (tile, shard batch) units:
-// while one batch is added, the loads of the next unit (the next batch of
-// this tile, or the first batch of the warp's next tile) are in flight, in the
-// other of two register buffers, so nothing is copied.
-template <int FIN, int FOUT, int KU>
-__global__ void __launch_bounds__(kThreads, KU == 1 ? 3 : 2)
+template <int FIN, int FOUT>
+__global__ void __launch_bounds__(kRedThreads, 2)
     reduce_kernel(const __grid_constant__ ReduceArgs a) {
-  constexpr int kBatch = kBatchOf<FIN>;
-  constexpr int TILE = KU * kRun;
-  const WarpCursor c;
-  const int64_t nfull = a.n / TILE;
-  const int64_t stride = c.nwarps * TILE;
-  const int64_t end = nfull * TILE;
-  ShardBatch<FIN, KU> buf[2];
-  float acc[KU][kVec];
-  // cursors of the unit being added (e0, r0) and of the unit being loaded
-  int64_t e0 = c.warp * TILE, le0 = e0;
-  int r0 = 0, lr0 = 0;
-  auto advance = [&](int64_t &e, int &r) {
-    r += kBatch;
-    if (r >= a.nshards) {
-      r = 0;
-      e += stride;
+  using RG = RedGeom<FIN>;
+  constexpr int BIN = Fmt<FIN>::kBits, WIN = Fmt<FIN>::kWords16, CB = RG::kCodeBytes;
+  constexpr int S = RG::kStages;
+  extern __shared__ __align__(128) uint8_t red_smem[];
+  pdl_enter();
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const uint32_t full0 = smem_addr(red_smem + RG::kBarOff), empty0 = full0 + 8 * S;
+  const int64_t nfull = a.n / kTile;                                 // whole 1024-element tiles
+  const int64_t nct = (nfull + kRedConsumers - 1) / kRedConsumers;   // CTA tiles
+  const int nb = (a.nshards + RG::kShards - 1) / RG::kShards;        // units per CTA tile
+  const int64_t mytiles =
+      blockIdx.x < nct ? (nct - 1 - int64_t(blockIdx.x)) / gridDim.x + 1 : 0;
+  const int64_t nunits = mytiles * nb;
+  const int lgin = a.log2Gin;
+  const int nbt = kTile >> lgin;  // input blocks per tile
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int st = 0; st < S; ++st) {
+      mbar_init(full0 + 8 * st, 1);
+      mbar_init(empty0 + 8 * st, kRedConsumers);
     }
-  };
-  if (le0 < end) {
-    load_batch<FIN, KU>(a, le0, lr0, c.lane, buf[0]);
-    advance(le0, lr0);
+    mbar_init_fence();
   }
-  while (e0 < end) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {  // h: the buffer that holds the unit (e0, r0)
-      if (e0 < end) {
-        if (le0 < end) {
-          load_batch<FIN, KU>(a, le0, lr0, c.lane, buf[h ^ 1]);
-          advance(le0, lr0);
-        }
-        if (r0 == 0) {
-#pragma unroll
-          for (int j = 0; j < KU; ++j)
-#pragma unroll
-            for (int v = 0; v < kVec; ++v) acc[j][v] = 0.0f;
-        }
-        add_batch<FIN, KU>(a, r0, buf[h], acc);
-        if (r0 + kBatch >= a.nshards) {  // last batch of the tile
-          if (a.sum_out) {
-#pragma unroll
-            for (int j = 0; j < KU; ++j)
-              store16<DT_F32>(a.sum_out, e0 + j * kRun + c.lane * kVec, acc[j], a.wide != 0);
-          }
-          requant_tile<FOUT, KU>(a, acc, e0, c.lane);
-        }
-        advance(e0, r0);
+  __syncthreads();
+
+  if (w == kRedConsumers) {  // producer warp: lane 0 issues every copy
+    if (lane != 0) return;
+    int64_t ct = blockIdx.x;  // cursor (ct, k) of unit u
+    int k = 0;
+    for (int64_t u = 0; u < nunits; ++u) {
+      const int st = int(u % S);
+      if (u >= S && !mbar_wait_thread(empty0 + 8 * st, uint32_t(u / S - 1) & 1u)) {
+        // Timed out: record it, wait (bounded) for the copies in flight, stop.
+        atomicOr(&g_dev_error, kDevErrWaitTimeout);
+        for (int64_t v = u - S; v < u; ++v)
+          (void)mbar_wait_thread(full0 + 8 * int(v % S), uint32_t(v / S) & 1u);
+        return;
+      }
+      const int r0 = k * RG::kShards;
+      const int ns = min(RG::kShards, a.nshards - r0);
+      const int64_t left = nfull - ct * kRedConsumers;
+      const int cnt = int(left < kRedConsumers ? left : kRedConsumers);
+      const uint32_t cbytes = uint32_t(cnt) * CB, sbytes = uint32_t(cnt * nbt) * 4u;
+      const bool stma = (sbytes % 16u) == 0u;
+      const uint32_t full = full0 + 8 * st;
+      const uint32_t dst = smem_addr(red_smem + st * RG::kStage);
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(full, uint32_t(ns) * (cbytes + (stma ? sbytes : 0u)));
+      for (int q = 0; q < ns; ++q) {
+        bulk_g2s(dst + q * kRedConsumers * CB, a.codes[r0 + q] + ct * kRedConsumers * CB, cbytes,
+                 full);
+        if (stma)
+          bulk_g2s(dst + RG::kScaleOff + q * kRedConsumers * nbt * 4,
+                   a.scales[r0 + q] + ct * kRedConsumers * nbt, sbytes, full);
+      }
+      if (++k == nb) {
+        k = 0;
+        ct += gridDim.x;
       }
     }
+    return;
   }
-  // the partial last tile goes to the warp that would take tile n / TILE
-  if ((a.n % TILE) != 0 && c.warp == nfull % c.nwarps) reduce_tail<FIN, FOUT>(a, end, c.lane);
+
+  // consumer warp w: tile w of every CTA tile
+  float acc[kU][kVec];
+  int64_t ct = blockIdx.x;  // cursor (ct, k) of unit u
+  int k = 0;
+  for (int64_t u = 0; u < nunits; ++u) {
+    const int st = int(u % S);
+    if (!mbar_wait_warp(full0 + 8 * st, uint32_t(u / S) & 1u)) {
+      if (lane == 0) atomicOr(&g_dev_error, kDevErrWaitTimeout);
+      return;
+    }
+    const int r0 = k * RG::kShards;
+    const int ns = min(RG::kShards, a.nshards - r0);
+    const int64_t left = nfull - ct * kRedConsumers;
+    const int cnt = int(left < kRedConsumers ? left : kRedConsumers);
+    const bool stma = ((cnt * nbt * 4) % 16) == 0;
+    const int64_t e0 = (ct * kRedConsumers + w) * kTile;
+    if (k == 0) {
+#pragma unroll
+      for (int j = 0; j < kU; ++j)
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) acc[j][v] = 0.0f;
+    }
+    if (w < cnt) {
+      const uint8_t *sb = red_smem + st * RG::kStage;
+      if (stma) {  // scales in the stage
+#pragma unroll
+        for (int q = 0; q < RG::kShards; ++q) {
+          if (q < ns) {  // shard order is the summation order
+            const uint8_t *cq = sb + (q * kRedConsumers + w) * CB;
+            const float *sq = reinterpret_cast<const float *>(sb + RG::kScaleOff) +
+                              (q * kRedConsumers + w) * nbt;
+#pragma unroll
+            for (int j = 0; j < kU; ++j) {
+              const int off = j * kRun + lane * kVec;
+              uint32_t wv[WIN];
+              load_codes16_smem<BIN>(cq + off * BIN / 8, wv);
+              accumulate16<FIN>(acc[j], wv, sq[off >> lgin], a.one);
+            }
+          }
+        }
+      } else {  // scales from global memory (G_in >= 512 at the end of the tensor)
+        for (int q = 0; q < ns; ++q) {
+          const uint8_t *cq = sb + (q * kRedConsumers + w) * CB;
+          const float *sg = a.scales[r0 + q];
+#pragma unroll
+          for (int j = 0; j < kU; ++j) {
+            const int off = j * kRun + lane * kVec;
+            uint32_t wv[WIN];
+            load_codes16_smem<BIN>(cq + off * BIN / 8, wv);
+            accumulate16<FIN>(acc[j], wv, ld_nc_f32(sg + ((e0 + off) >> lgin)), a.one);
+          }
+        }
+      }
+    }
+    __syncwarp();  // every lane has read the stage
+    if (lane == 0) mbar_arrive(empty0 + 8 * st);
+    if (k == nb - 1 && w < cnt) {  // last unit of the tile
+      if (a.sum_out) {
+#pragma unroll
+        for (int j = 0; j < kU; ++j)
+          store16<DT_F32>(a.sum_out, e0 + j * kRun + lane * kVec, acc[j], a.wide != 0);
+      }
+      requant_tile<FOUT, kU>(a, acc, e0, lane);
+    }
+    if (++k == nb) {
+      k = 0;
+      ct += gridDim.x;
+    }
+  }
+  // the partial last tile (fewer than 1024 elements) goes to warp 0 of CTA 0
+  if ((a.n % kTile) != 0 && blockIdx.x == 0 && w == 0) reduce_tail<FIN, FOUT>(a, nfull * kTile, lane);
 }
 
 // ===========================================================================

@@ -72,7 +72,7 @@ typedef enum zq_status {
     ZQ_ERR_MISALIGNED = 3,  /* a data pointer is not 16-byte aligned */
     ZQ_ERR_ALIAS = 4,       /* an output overlaps an input */
     ZQ_ERR_CUDA = 5,        /* the CUDA runtime reported an error (see zq_last_cuda_error) */
-    ZQ_ERR_TIMEOUT = 6      /* reserved: a bounded device-side wait ran out */
+    ZQ_ERR_TIMEOUT = 6      /* a bounded device-side wait ran out (see zq_device_status) */
 } zq_status;
 
 /* Element types of uncompressed tensors. */
@@ -151,6 +151,19 @@ zq_status zq_reduce_quantized(const void *const *codes, const float *const *scal
  */
 zq_status zq_fp8_accumulate(void *main_codes, float *main_scales, const void *grad, int grad_dtype,
                             int64_t n, int64_t G, void *stream);
+
+/*
+ * zq_device_status -- errors the kernels found on the device. The reduce
+ * kernels stream shard tiles into shared memory with bulk asynchronous copies
+ * and wait for them with a time limit (2 s); a wait that runs out stops that
+ * warp's work (its outputs are then incomplete) and sets a device error word
+ * instead of hanging the GPU. This call waits for `stream` to finish
+ * (cudaStreamSynchronize), reads and clears the error words of all kernels,
+ * and returns ZQ_ERR_TIMEOUT if any wait ran out since the last call,
+ * ZQ_ERR_CUDA if the stream reported a CUDA error, and ZQ_OK otherwise.
+ * (A library-side check with no counterpart on the pages.)
+ */
+zq_status zq_device_status(void *stream);
 
 /* Static description of a status code. */
 const char *zq_status_string(int status);

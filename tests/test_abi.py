@@ -30,7 +30,8 @@ def L():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for f in ("zq_quantize", "zq_dequantize", "zq_reduce_quantized", "zq_fp8_accumulate",
-              "zq_codes_bytes", "zq_num_blocks", "zq_status_string", "zq_last_cuda_error"):
+              "zq_codes_bytes", "zq_num_blocks", "zq_status_string", "zq_last_cuda_error",
+              "zq_device_status"):
         assert f in names
 
 

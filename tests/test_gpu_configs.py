@@ -121,6 +121,7 @@ def test_qgz_reduce_full(zq):
         del x
     for fout, Gout in ((zq.INT4, 128), (zq.INT8, 256)):
         oc, os_, sm = zq.reduce_quantized(codes, scales, n, zq.INT4, 128, fout, Gout, sum_out=True)
+        zq.device_status()
         hoc, hos, hsm = to_host(oc), to_host(os_), to_host(sm)
         for k, lo in enumerate(wins):
             sh = [O.quantize(xw, O.INT4, 128) for xw in host_win[k]]

@@ -162,6 +162,37 @@ def test_quantize_subnormal_scales(zq):
     assert_same_codes(codes, want_c, "codes clamp")
 
 
+def test_quantize_extreme_scales(zq):
+    """fp32 blocks whose scale sits at the edges of the fast paths: near the
+    largest binary32, around 2^126 (above it the reciprocal is subnormal and
+    the run must take the exact path), around 2^-100 (below it the block
+    scale and the fix-up use the IEEE division) and near 2^-126. Each block
+    holds random values and exact half-integer multiples of a power of two."""
+    rng = np.random.default_rng(11)
+    G = 32
+    s_targets = [3.0e38, 2.0 ** 127, 1.5 * 2.0 ** 126, 2.0 ** 126, 0.999 * 2.0 ** 126,
+                 2.0 ** 100, 1.0, 2.0 ** -99, 2.0 ** -100, 0.999 * 2.0 ** -100, 2.0 ** -120,
+                 2.0 ** -125, 1.001 * 2.0 ** -126, 2.0 ** -126]
+    for fmt in FORMATS:
+        d = 448.0 if fmt == O.E4M3 else float((1 << (O.BITS[fmt] - 1)) - 1)
+        blocks = []
+        for st in s_targets:
+            m = min(st * d, 3.4e38)
+            v = rng.standard_normal(G)
+            blocks.append((v / np.abs(v).max() * m).astype(np.float32))
+            p2 = 2.0 ** np.floor(np.log2(m / d))  # a power of two near the scale
+            k = rng.integers(-int(d), int(d), G) + 0.5
+            t = np.clip(k * p2, -3.4e38, 3.4e38).astype(np.float32)
+            t[0] = np.float32(min(d * p2, 3.4e38))
+            blocks.append(t)
+        x = np.concatenate(blocks)
+        assert np.all(np.isfinite(x))
+        codes, scales = gpu_quantize(zq, x, O.F32, fmt, G)
+        want_c, want_s = O.quantize(x, fmt, G)
+        assert_same_bits(scales, want_s, f"scales {fid(fmt)}")
+        assert_same_codes(codes, want_c, f"codes {fid(fmt)}")
+
+
 def test_quantize_unaligned_32B_source(zq):
     """A source that is 16- but not 32-byte aligned takes the 128-bit load path."""
     import torch
@@ -227,6 +258,7 @@ def _gpu_reduce(zq, shards, n, fin, Gin, fout, Gout, want_sum=True):
     scales = [bytes_dev(s) for _, s in shards]
     oc, os_, sm = zq.reduce_quantized(codes, scales, n, fin, Gin, fout, Gout,
                                       sum_out=True if want_sum else None)
+    zq.device_status()  # no bounded device-side wait ran out
     return to_host(oc), to_host(os_), (to_host(sm) if want_sum else None)
 
 
