@@ -27,6 +27,7 @@ FORMATS = (INT2, INT4, INT6, INT8, E4M3)
 BLOCK_SIZES = (32, 64, 128, 256, 512, 1024)
 BITS = {INT2: 2, INT4: 4, INT6: 6, INT8: 8, E4M3: 8}
 MAX_SHARDS = 64
+STATIC_MAX_SHARDS = 1024
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libzq.so")
 
@@ -55,6 +56,8 @@ def _declare(L):
     L.zq_quantize.argtypes = [vp, i32, i64, i32, i64, vp, vp, vp]
     L.zq_dequantize.argtypes = [vp, vp, i64, i32, i64, vp, i32, vp]
     L.zq_reduce_quantized.argtypes = [vp, vp, i32, i64, i32, i64, vp, vp, i32, i64, vp, vp]
+    L.zq_reduce_quantized_static.argtypes = [vp, vp, i32, i64, i32, i64, vp, vp, i32, i64, vp, vp]
+    L.zq_reduce_quantized_static.restype = i32
     L.zq_fp8_accumulate.argtypes = [vp, vp, vp, i32, i64, i64, vp]
     for f in ("zq_quantize", "zq_dequantize", "zq_reduce_quantized", "zq_fp8_accumulate"):
         getattr(L, f).restype = i32
@@ -160,12 +163,8 @@ def dequantize(codes, scales, n: int, fmt: int, G: int, out_dtype=None, out=None
     return out
 
 
-def reduce_quantized(codes_list, scales_list, n: int, fmt_in: int, G_in: int, fmt_out: int,
-                     G_out: int, out_codes=None, out_scales=None, sum_out=None, stream=None):
-    """Shard-ordered fp32 sum of N quantized shards, requantized.
-
-    ``sum_out``: None (not written), True (allocate), or an fp32 tensor of n.
-    Returns (out_codes, out_scales, sum_out_or_None)."""
+def _reduce(entry: str, codes_list, scales_list, n, fmt_in, G_in, fmt_out, G_out, out_codes,
+            out_scales, sum_out, stream):
     torch = _torch()
     N = len(codes_list)
     if N != len(scales_list):
@@ -177,11 +176,32 @@ def reduce_quantized(codes_list, scales_list, n: int, fmt_in: int, G_in: int, fm
         sum_out = torch.empty(n, dtype=torch.float32, device=dev)
     cp = (ctypes.c_void_p * N)(*[c.data_ptr() for c in codes_list])
     sp = (ctypes.c_void_p * N)(*[s.data_ptr() for s in scales_list])
-    _check(lib().zq_reduce_quantized(cp, sp, N, n, fmt_in, G_in, out_codes.data_ptr(),
-                                     out_scales.data_ptr(), fmt_out, G_out,
-                                     sum_out.data_ptr() if sum_out is not None else None,
-                                     _stream(out_codes, stream)), "zq_reduce_quantized")
+    _check(getattr(lib(), entry)(cp, sp, N, n, fmt_in, G_in, out_codes.data_ptr(),
+                                 out_scales.data_ptr(), fmt_out, G_out,
+                                 sum_out.data_ptr() if sum_out is not None else None,
+                                 _stream(out_codes, stream)), entry)
     return out_codes, out_scales, sum_out
+
+
+def reduce_quantized(codes_list, scales_list, n: int, fmt_in: int, G_in: int, fmt_out: int,
+                     G_out: int, out_codes=None, out_scales=None, sum_out=None, stream=None):
+    """Shard-ordered fp32 sum of N quantized shards, requantized.
+
+    ``sum_out``: None (not written), True (allocate), or an fp32 tensor of n.
+    Returns (out_codes, out_scales, sum_out_or_None)."""
+    return _reduce("zq_reduce_quantized", codes_list, scales_list, n, fmt_in, G_in, fmt_out,
+                   G_out, out_codes, out_scales, sum_out, stream)
+
+
+def reduce_quantized_static(codes_list, scales_list, n: int, fmt_in: int, G_in: int,
+                            fmt_out: int, G_out: int, out_codes=None, out_scales=None,
+                            sum_out=None, stream=None):
+    """reduce_quantized for up to 1024 shards through zq_reduce_quantized_static,
+    which allocates nothing (its shard table is a static device array shared by
+    all calls: calls that overlap on the GPU race). Outputs are allocated here
+    only when not given; a caller that cannot allocate passes them in."""
+    return _reduce("zq_reduce_quantized_static", codes_list, scales_list, n, fmt_in, G_in,
+                   fmt_out, G_out, out_codes, out_scales, sum_out, stream)
 
 
 def fp8_accumulate(main_codes, main_scales, grad, G: int, stream=None):

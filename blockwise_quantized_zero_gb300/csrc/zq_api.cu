@@ -114,6 +114,46 @@ int device_sm_count() {
   return g_sm_count[dev];
 }
 
+// Argument checks shared by the two reduce entry points (they differ only in
+// the largest shard count); ZQ_OK with n == 0 means "nothing to do".
+static zq_status check_reduce(const void *const *codes, const float *const *scales, int nshards,
+                       int max_shards, int64_t n, int format_in, int64_t G_in,
+                       const void *out_codes, const float *out_scales, int format_out,
+                       int64_t G_out, const float *sum_out) {
+  if (!bits_of(format_in) || !bits_of(format_out)) return ZQ_ERR_UNSUPPORTED;
+  if (n < 0 || !valid_block(G_in) || !valid_block(G_out) || nshards < 1 || nshards > max_shards)
+    return ZQ_ERR_INVALID_ARG;
+  if (n == 0) return ZQ_OK;
+  if (!codes || !scales || !out_codes || !out_scales) return ZQ_ERR_INVALID_ARG;
+  for (int r = 0; r < nshards; ++r)
+    if (!codes[r] || !scales[r]) return ZQ_ERR_INVALID_ARG;
+  for (int r = 0; r < nshards; ++r)
+    if (!aligned16(codes[r]) || !aligned16(scales[r])) return ZQ_ERR_MISALIGNED;
+  if (!aligned16(out_codes) || !aligned16(out_scales) || (sum_out && !aligned16(sum_out)))
+    return ZQ_ERR_MISALIGNED;
+  const Range oc(out_codes, zq_codes_bytes(format_out, n)),
+      os(out_scales, size_t(zq_num_blocks(n, G_out)) * 4u),
+      sm(sum_out, sum_out ? size_t(n) * 4u : 0u);
+  if (oc.overlaps(os) || oc.overlaps(sm) || os.overlaps(sm)) return ZQ_ERR_ALIAS;
+  for (int r = 0; r < nshards; ++r) {
+    const Range ic(codes[r], zq_codes_bytes(format_in, n)),
+        is(scales[r], size_t(zq_num_blocks(n, G_in)) * 4u);
+    for (const Range *o : {&oc, &os, &sm})
+      if (o->overlaps(ic) || o->overlaps(is)) return ZQ_ERR_ALIAS;
+  }
+  for (int r = 0; r < nshards; ++r) {
+    if (zq_status st = check_device_ptr(codes[r])) return st;
+    if (zq_status st = check_device_ptr(scales[r])) return st;
+  }
+  if (zq_status st = check_device_ptr(out_codes)) return st;
+  if (zq_status st = check_device_ptr(out_scales)) return st;
+  if (sum_out)
+    if (zq_status st = check_device_ptr(sum_out)) return st;
+  return ZQ_OK;
+}
+
+static_assert(ZQ_STATIC_MAX_SHARDS == kStaticMaxShards, "shard table size");
+
 }  // namespace zq
 
 using namespace zq;
@@ -192,40 +232,15 @@ zq_status zq_dequantize(const void *codes, const float *scales, int64_t n, int f
                                      as_stream(stream), wide));
 }
 
+
 zq_status zq_reduce_quantized(const void *const *codes, const float *const *scales, int nshards,
                               int64_t n, int format_in, int64_t G_in, void *out_codes,
                               float *out_scales, int format_out, int64_t G_out, float *sum_out,
                               void *stream) {
-  if (!bits_of(format_in) || !bits_of(format_out)) return ZQ_ERR_UNSUPPORTED;
-  if (n < 0 || !valid_block(G_in) || !valid_block(G_out) || nshards < 1 ||
-      nshards > ZQ_MAX_SHARDS)
-    return ZQ_ERR_INVALID_ARG;
+  if (zq_status st = check_reduce(codes, scales, nshards, ZQ_MAX_SHARDS, n, format_in, G_in,
+                                  out_codes, out_scales, format_out, G_out, sum_out))
+    return st;
   if (n == 0) return ZQ_OK;
-  if (!codes || !scales || !out_codes || !out_scales) return ZQ_ERR_INVALID_ARG;
-  for (int r = 0; r < nshards; ++r)
-    if (!codes[r] || !scales[r]) return ZQ_ERR_INVALID_ARG;
-  for (int r = 0; r < nshards; ++r)
-    if (!aligned16(codes[r]) || !aligned16(scales[r])) return ZQ_ERR_MISALIGNED;
-  if (!aligned16(out_codes) || !aligned16(out_scales) || (sum_out && !aligned16(sum_out)))
-    return ZQ_ERR_MISALIGNED;
-  const Range oc(out_codes, zq_codes_bytes(format_out, n)),
-      os(out_scales, size_t(zq_num_blocks(n, G_out)) * 4u),
-      sm(sum_out, sum_out ? size_t(n) * 4u : 0u);
-  if (oc.overlaps(os) || oc.overlaps(sm) || os.overlaps(sm)) return ZQ_ERR_ALIAS;
-  for (int r = 0; r < nshards; ++r) {
-    const Range ic(codes[r], zq_codes_bytes(format_in, n)),
-        is(scales[r], size_t(zq_num_blocks(n, G_in)) * 4u);
-    for (const Range *o : {&oc, &os, &sm})
-      if (o->overlaps(ic) || o->overlaps(is)) return ZQ_ERR_ALIAS;
-  }
-  for (int r = 0; r < nshards; ++r) {
-    if (zq_status st = check_device_ptr(codes[r])) return st;
-    if (zq_status st = check_device_ptr(scales[r])) return st;
-  }
-  if (zq_status st = check_device_ptr(out_codes)) return st;
-  if (zq_status st = check_device_ptr(out_scales)) return st;
-  if (sum_out)
-    if (zq_status st = check_device_ptr(sum_out)) return st;
 
   ReduceArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -243,6 +258,30 @@ zq_status zq_reduce_quantized(const void *const *codes, const float *const *scal
   a.wide = (!sum_out || aligned32(sum_out)) ? 1 : 0;
   a.one = 1.0f;
   return from_cuda(launch_reduce(a, format_in, format_out, as_stream(stream)));
+}
+
+zq_status zq_reduce_quantized_static(const void *const *codes, const float *const *scales,
+                                     int nshards, int64_t n, int format_in, int64_t G_in,
+                                     void *out_codes, float *out_scales, int format_out,
+                                     int64_t G_out, float *sum_out, void *stream) {
+  if (zq_status st = check_reduce(codes, scales, nshards, ZQ_STATIC_MAX_SHARDS, n, format_in,
+                                  G_in, out_codes, out_scales, format_out, G_out, sum_out))
+    return st;
+  if (n == 0) return ZQ_OK;
+
+  TableReduceArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.out_codes = static_cast<uint8_t *>(out_codes);
+  a.out_scales = out_scales;
+  a.sum_out = sum_out;
+  a.n = n;
+  a.nshards = nshards;
+  a.log2Gin = log2_block(G_in);
+  a.log2Gout = log2_block(G_out);
+  a.wide = (!sum_out || aligned32(sum_out)) ? 1 : 0;
+  a.one = 1.0f;
+  return from_cuda(launch_reduce_static(codes, scales, a, format_in, format_out,
+                                        as_stream(stream)));
 }
 
 zq_status zq_fp8_accumulate(void *main_codes, float *main_scales, const void *grad, int grad_dtype,

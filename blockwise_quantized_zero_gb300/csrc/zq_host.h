@@ -76,6 +76,10 @@ cudaError_t launch_quantize(const void *src, int dt, int64_t n, int fmt, int64_t
 cudaError_t launch_dequantize(const void *codes, const float *scales, int64_t n, int fmt,
                               int64_t G, void *dst, int dt, cudaStream_t st, bool wide);
 cudaError_t launch_reduce(const ReduceArgs &a, int fin, int fout, cudaStream_t st);
+// The same reduce with up to kStaticMaxShards shards whose pointers (host
+// arrays) are copied into a static device table on the stream.
+cudaError_t launch_reduce_static(const void *const *codes, const float *const *scales,
+                                 const TableReduceArgs &args, int fin, int fout, cudaStream_t st);
 // Reads and clears the device error words of the launch units.
 unsigned take_reduce_device_error();
 

@@ -323,6 +323,30 @@ struct ReduceArgs {
   int log2Gout;
   int wide;
   float one;  // 1.0f, passed at run time (see accumulate16)
+  __device__ const uint8_t *shard_codes(int r) const { return codes[r]; }
+  __device__ const float *shard_scales(int r) const { return scales[r]; }
+};
+
+// The same arguments with the shard pointers in a device-memory table instead
+// of the kernel parameters (up to kStaticMaxShards shards).
+constexpr int kStaticMaxShards = 1024;
+struct ShardTable {
+  const uint8_t *codes[kStaticMaxShards];
+  const float *scales[kStaticMaxShards];
+};
+struct TableReduceArgs {
+  const ShardTable *tab;
+  uint8_t *out_codes;
+  float *out_scales;
+  float *sum_out;
+  int64_t n;
+  int nshards;
+  int log2Gin;
+  int log2Gout;
+  int wide;
+  float one;
+  __device__ const uint8_t *shard_codes(int r) const { return tab->codes[r]; }
+  __device__ const float *shard_scales(int r) const { return tab->scales[r]; }
 };
 
 // Add shard r's 16 dequantized values into acc: acc = fl(acc + fl(q * s)).
@@ -348,8 +372,8 @@ __device__ __forceinline__ void accumulate16(float (&acc)[kVec],
 // tree over the G/16 lanes of a block; lane l then computes the scale (IEEE
 // division) and its reciprocal of block l of the tile, stores it, and the
 // lanes of each block fetch them back with a shuffle.
-template <int FOUT, int KU>
-__device__ __forceinline__ void requant_tile(const ReduceArgs &a, float (&acc)[KU][kVec],
+template <int FOUT, int KU, typename A>
+__device__ __forceinline__ void requant_tile(const A &a, float (&acc)[KU][kVec],
                                              int64_t e0, int lane) {
   constexpr int B = Fmt<FOUT>::kBits, W = Fmt<FOUT>::kWords16;
   const int lg = a.log2Gout;                 // 5 .. 10, and G <= KU * 512
@@ -397,15 +421,15 @@ __device__ __forceinline__ void requant_tile(const ReduceArgs &a, float (&acc)[K
 }
 
 // Sum over shards of element i (tails).
-template <int FIN> __device__ __forceinline__ float reduce1(const ReduceArgs &a, int64_t i) {
+template <int FIN, typename A> __device__ __forceinline__ float reduce1(const A &a, int64_t i) {
   float acc = 0.0f;
   for (int r = 0; r < a.nshards; ++r)
-    acc = __fadd_rn(acc, dequant1<FIN>(a.codes[r], i, a.scales[r][i >> a.log2Gin]));
+    acc = __fadd_rn(acc, dequant1<FIN>(a.shard_codes(r), i, a.shard_scales(r)[i >> a.log2Gin]));
   return acc;
 }
 
-template <int FIN, int FOUT>
-__device__ __noinline__ void reduce_tail(const ReduceArgs &a, int64_t e0, int lane) {
+template <int FIN, int FOUT, typename A>
+__device__ __noinline__ void reduce_tail(const A &a, int64_t e0, int lane) {
   constexpr int B = Fmt<FOUT>::kBits;
   const int64_t n = a.n, Gout = int64_t(1) << a.log2Gout;
   uint32_t *cw = reinterpret_cast<uint32_t *>(a.out_codes);
@@ -413,7 +437,7 @@ __device__ __noinline__ void reduce_tail(const ReduceArgs &a, int64_t e0, int la
     const int64_t hi = (lo + Gout < n) ? lo + Gout : n;
     float m = 0.0f;
     for (int64_t i = lo + lane; i < hi; i += 32) {
-      const float v = reduce1<FIN>(a, i);
+      const float v = reduce1<FIN, A>(a, i);
       if (a.sum_out) a.sum_out[i] = v;
       m = fmaxf(m, fabsf(v));
     }
@@ -425,7 +449,7 @@ __device__ __noinline__ void reduce_tail(const ReduceArgs &a, int64_t e0, int la
       const int64_t last = ((bit0 + 32 + B - 1) / B < len) ? (bit0 + 32 + B - 1) / B : len;
       uint32_t word = 0;
       for (int64_t e = first; e < last; ++e) {
-        const uint32_t c = code1_exact<FOUT>(reduce1<FIN>(a, lo + e), s);
+        const uint32_t c = code1_exact<FOUT>(reduce1<FIN, A>(a, lo + e), s);
         const int sh = static_cast<int>(e * B - bit0);
         word |= (sh >= 0) ? (c << sh) : (c >> (-sh));
       }
@@ -486,9 +510,9 @@ template <int FIN> struct RedGeom {
 // Device error word of this translation unit (read by zq_device_status).
 static __device__ unsigned int g_dev_error = 0;
 
-template <int FIN, int FOUT>
+template <int FIN, int FOUT, typename A>
 __global__ void __launch_bounds__(kRedThreads, 2)
-    reduce_kernel(const __grid_constant__ ReduceArgs a) {
+    reduce_kernel(const __grid_constant__ A a) {
   using RG = RedGeom<FIN>;
   constexpr int BIN = Fmt<FIN>::kBits, WIN = Fmt<FIN>::kWords16, CB = RG::kCodeBytes;
   constexpr int S = RG::kStages;
@@ -539,11 +563,11 @@ __global__ void __launch_bounds__(kRedThreads, 2)
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(full, uint32_t(ns) * (cbytes + (stma ? sbytes : 0u)));
       for (int q = 0; q < ns; ++q) {
-        bulk_g2s(dst + q * kRedConsumers * CB, a.codes[r0 + q] + ct * kRedConsumers * CB, cbytes,
+        bulk_g2s(dst + q * kRedConsumers * CB, a.shard_codes(r0 + q) + ct * kRedConsumers * CB, cbytes,
                  full);
         if (stma)
           bulk_g2s(dst + RG::kScaleOff + q * kRedConsumers * nbt * 4,
-                   a.scales[r0 + q] + ct * kRedConsumers * nbt, sbytes, full);
+                   a.shard_scales(r0 + q) + ct * kRedConsumers * nbt, sbytes, full);
       }
       if (++k == nb) {
         k = 0;
@@ -596,7 +620,7 @@ __global__ void __launch_bounds__(kRedThreads, 2)
       } else {  // scales from global memory (G_in >= 512 at the end of the tensor)
         for (int q = 0; q < ns; ++q) {
           const uint8_t *cq = sb + (q * kRedConsumers + w) * CB;
-          const float *sg = a.scales[r0 + q];
+          const float *sg = a.shard_scales(r0 + q);
 #pragma unroll
           for (int j = 0; j < kU; ++j) {
             const int off = j * kRun + lane * kVec;
@@ -615,7 +639,7 @@ __global__ void __launch_bounds__(kRedThreads, 2)
         for (int j = 0; j < kU; ++j)
           store16<DT_F32>(a.sum_out, e0 + j * kRun + lane * kVec, acc[j], a.wide != 0);
       }
-      requant_tile<FOUT, kU>(a, acc, e0, lane);
+      requant_tile<FOUT, kU, A>(a, acc, e0, lane);
     }
     if (++k == nb) {
       k = 0;
@@ -623,7 +647,8 @@ __global__ void __launch_bounds__(kRedThreads, 2)
     }
   }
   // the partial last tile (fewer than 1024 elements) goes to warp 0 of CTA 0
-  if ((a.n % kTile) != 0 && blockIdx.x == 0 && w == 0) reduce_tail<FIN, FOUT>(a, nfull * kTile, lane);
+  if ((a.n % kTile) != 0 && blockIdx.x == 0 && w == 0)
+    reduce_tail<FIN, FOUT, A>(a, nfull * kTile, lane);
 }
 
 // ===========================================================================

@@ -1,14 +1,17 @@
 // zq_reduce.cu -- launch unit for the quantized-reduce kernels (one
 // instantiation per input and output code format), and the reader of the
 // reduce kernels' device error word.
+#include <cstddef>
+#include <mutex>
+
 #include "zq_host.h"
 
 namespace zq {
 
 // Persistent grid of CTAs of eight consumer warps and one producer warp: one
 // CTA per CTA tile (8192 elements), at most one wave.
-template <int FIN, int FOUT> static cudaError_t go_r(const ReduceArgs &a, cudaStream_t st) {
-  constexpr auto K = reduce_kernel<FIN, FOUT>;
+template <int FIN, int FOUT, typename A> static cudaError_t go_r(const A &a, cudaStream_t st) {
+  constexpr auto K = reduce_kernel<FIN, FOUT, A>;
   constexpr int kSmem = RedGeom<FIN>::kSmem;
   const int occ = ctas_per_sm<K, kSmem, kRedThreads>();
   if (occ < 1) return cudaErrorInvalidConfiguration;
@@ -19,7 +22,7 @@ template <int FIN, int FOUT> static cudaError_t go_r(const ReduceArgs &a, cudaSt
   return launch_pdl_threads(K, grid, kRedThreads, kSmem, st, a);
 }
 
-template <int FIN> static cudaError_t go_r_o(const ReduceArgs &a, int fout, cudaStream_t st) {
+template <int FIN, typename A> static cudaError_t go_r_o(const A &a, int fout, cudaStream_t st) {
   switch (fout) {
     case F_INT2: return go_r<FIN, F_INT2>(a, st);
     case F_INT4: return go_r<FIN, F_INT4>(a, st);
@@ -30,7 +33,7 @@ template <int FIN> static cudaError_t go_r_o(const ReduceArgs &a, int fout, cuda
   }
 }
 
-cudaError_t launch_reduce(const ReduceArgs &a, int fin, int fout, cudaStream_t st) {
+template <typename A> static cudaError_t go_r_io(const A &a, int fin, int fout, cudaStream_t st) {
   switch (fin) {
     case F_INT2: return go_r_o<F_INT2>(a, fout, st);
     case F_INT4: return go_r_o<F_INT4>(a, fout, st);
@@ -39,6 +42,64 @@ cudaError_t launch_reduce(const ReduceArgs &a, int fin, int fout, cudaStream_t s
     case F_E4M3: return go_r_o<F_E4M3>(a, fout, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_reduce(const ReduceArgs &a, int fin, int fout, cudaStream_t st) {
+  return go_r_io(a, fin, fout, st);
+}
+
+// ---------------------------------------------------------------------------
+// The allocation-free variant for many shards. The shard pointer table lives
+// in this file-scope device array (16 KiB, held by every GPU that loads the
+// library until the process exits). Its name in host code is only a host-side
+// stand-in: the kernels get the device address, looked up once per device
+// with cudaGetSymbolAddress while that device is current (on the device's
+// first call). Every call overwrites the first nshards entries of both lists
+// with stream-ordered copies, and the kernel reads no other entry, so nothing
+// needs clearing. All calls share the table: calls whose work overlaps on the
+// GPU (different streams, not ordered) race on it.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) ShardTable g_shard_table;
+
+namespace {
+constexpr int kMaxTableDevices = 64;
+ShardTable *g_table_ptr[kMaxTableDevices] = {nullptr};
+std::mutex g_table_mutex;
+
+cudaError_t table_address(ShardTable **out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxTableDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_table_mutex);
+  if (!g_table_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_shard_table);
+    if (e != cudaSuccess) return e;
+    g_table_ptr[dev] = static_cast<ShardTable *>(p);
+  }
+  *out = g_table_ptr[dev];
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_reduce_static(const void *const *codes, const float *const *scales,
+                                 const TableReduceArgs &args, int fin, int fout,
+                                 cudaStream_t st) {
+  if (args.nshards < 1 || args.nshards > kStaticMaxShards) return cudaErrorInvalidValue;
+  ShardTable *tab = nullptr;
+  cudaError_t e = table_address(&tab);
+  if (e != cudaSuccess) return e;
+  const size_t bytes = size_t(args.nshards) * sizeof(void *);
+  char *base = reinterpret_cast<char *>(tab);  // device address: arithmetic only
+  e = cudaMemcpyAsync(base + offsetof(ShardTable, codes), codes, bytes, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyAsync(base + offsetof(ShardTable, scales), scales, bytes, cudaMemcpyHostToDevice,
+                      st);
+  if (e != cudaSuccess) return e;
+  TableReduceArgs a = args;
+  a.tab = tab;
+  return go_r_io(a, fin, fout, st);
 }
 
 unsigned take_reduce_device_error() {

@@ -90,6 +90,9 @@ typedef enum zq_format {
 /* Largest shard count accepted by zq_reduce_quantized. */
 #define ZQ_MAX_SHARDS 64
 
+/* Largest shard count accepted by zq_reduce_quantized_static. */
+#define ZQ_STATIC_MAX_SHARDS 1024
+
 /* Bytes of the packed code stream for n elements: ceil(n * bits / 32) * 4.
  * With n a multiple of G this is n * b / 8 ([Aquavit] Eq. 6 without the
  * metadata term). Returns 0 for an unknown format or n < 0. Host only. */
@@ -138,6 +141,34 @@ zq_status zq_reduce_quantized(const void *const *codes, const float *const *scal
                               int64_t n, int format_in, int64_t G_in, void *out_codes,
                               float *out_scales, int format_out, int64_t G_out, float *sum_out,
                               void *stream);
+
+/*
+ * zq_reduce_quantized_static -- zq_reduce_quantized for more shards than fit
+ * in kernel parameters (up to ZQ_STATIC_MAX_SHARDS = 1024), without allocating
+ * anything. There is no counterpart on the pages: this is a library entry point
+ * for callers that cannot allocate device memory themselves or let a library do
+ * it -- e.g. code whose device memory is entirely owned by another allocator (a
+ * framework's caching allocator that has reserved most of HBM, where a stray
+ * cudaMalloc can fail or fragment the pool), or a runtime that forbids
+ * allocation on its hot path. The shard pointer table that a many-shard reduce
+ * needs in device memory lives in a static 16 KiB device array that every GPU
+ * which loads the library holds until the process exits.
+ * Arguments, results and errors are those of zq_reduce_quantized, except:
+ *   nshards   1 .. ZQ_STATIC_MAX_SHARDS; a larger count returns
+ *             ZQ_ERR_INVALID_ARG with nothing enqueued.
+ *   codes[r], scales[r]  HOST arrays, copied into the device table on `stream`
+ *             (stream-ordered copies from host memory) during the call.
+ * The first call on a device looks up the table's device address with
+ * cudaGetSymbolAddress (with that device current); make that first call before
+ * any stream capture. All calls share the one table: calls whose work overlaps
+ * on the GPU (e.g. on two streams that are not ordered) race on it and must not
+ * be issued; calls on one stream are ordered and safe. It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ */
+zq_status zq_reduce_quantized_static(const void *const *codes, const float *const *scales,
+                                     int nshards, int64_t n, int format_in, int64_t G_in,
+                                     void *out_codes, float *out_scales, int format_out,
+                                     int64_t G_out, float *sum_out, void *stream);
 
 /*
  * zq_fp8_accumulate -- in-place FP8 gradient accumulation ([AGoQ] 2.B "Local

@@ -116,6 +116,24 @@ def test_reduce_argument_errors(L):
     assert r(os=oc + 16) == ALIAS
 
 
+def test_static_reduce_shard_limit(L):
+    """zq_reduce_quantized_static takes up to ZQ_STATIC_MAX_SHARDS shards and
+    refuses more before any work (n = 0 stops after the argument checks)."""
+    N = zq.STATIC_MAX_SHARDS + 1
+    cp = (ctypes.c_void_p * N)(*[BASE + i * (1 << 20) for i in range(N)])
+    sp = (ctypes.c_void_p * N)(*[BASE + (1 << 31) + i * (1 << 20) for i in range(N)])
+    oc, os_, sm = BASE + (1 << 33), BASE + (1 << 34), BASE + (1 << 35)
+
+    def r(entry, nshards, n):
+        return getattr(L, entry)(cp, sp, nshards, n, zq.INT4, 128, oc, os_, zq.INT4, 128, sm, None)
+
+    assert r("zq_reduce_quantized_static", N, 4096) == INVALID
+    assert r("zq_reduce_quantized_static", 0, 4096) == INVALID
+    assert r("zq_reduce_quantized_static", N - 1, 0) == OK
+    assert r("zq_reduce_quantized_static", 65, 0) == OK
+    assert r("zq_reduce_quantized", 65, 0) == INVALID
+
+
 def test_fp8_accumulate_argument_errors(L):
     c, s, g = BASE, BASE + (1 << 24), BASE + (1 << 26)
     assert L.zq_fp8_accumulate(c, s, g, 5, 4096, 128, None) == UNSUPPORTED
