@@ -149,6 +149,7 @@ class GMSweep:
     """8192x8192 bf16 ~ N(0, 0.02); b in {2,4,6,8} x G in {1024..32}; Q then D -> bf16."""
 
     name = "gm_sweep"
+    dtype = "bf16 in, int2/4/6/8 codes + fp32 scales, bf16 out (fp32 arithmetic)"
     rows, cols = 8192, 8192
     bits = (2, 4, 6, 8)
     blocks = (1024, 512, 256, 128, 64, 32)
@@ -264,9 +265,11 @@ class QwzFP16:
     latency is reported beside it."""
 
     name = "qwz_fp16"
+    dtype = "fp16 in, int8 codes + fp32 scales, fp32 out (fp32 arithmetic)"
     copies = 512
     n = 1 << 20
     G = 256
+    streams = 8  # the graph's independent calls run as this many concurrent chains
 
     def __init__(self):
         from blockwise_quantized_zero_gb300 import inputs
@@ -276,8 +279,9 @@ class QwzFP16:
     def config(self):
         return {"workload": "qwz_fp16: one fp16 tensor of 1,048,576 elements N(0,0.02) with 0.1% "
                             "outliers x50 (seed 0), int8 G=256 quantize + dequantize->fp32; "
-                            "timed as CUDA graphs of 512 calls on 512 distinct copies",
+                            "timed as CUDA graphs of 512 independent calls on 512 distinct copies",
                 "elements": self.n, "batched_copies": self.copies,
+                "graph_chains": self.streams,
                 "l2": "no flush: 512 distinct buffers per graph (1.6-2.7 GB per replay)",
                 "single_call_us": getattr(self, "single_call_us", None)}
 
@@ -308,12 +312,25 @@ class QwzFP16:
                 zq.quantize(self.src[i], zq.INT8, self.G, self.codes[i], self.scales[i])
                 zq.dequantize(self.codes[i], self.scales[i], self.n, zq.INT8, self.G, out=self.out[i])
         torch.cuda.synchronize()
-        with torch.cuda.graph(self.gq, stream=s):
-            for i in range(self.copies):
-                zq.quantize(self.src[i], zq.INT8, self.G, self.codes[i], self.scales[i])
-        with torch.cuda.graph(self.gd, stream=s):
-            for i in range(self.copies):
-                zq.dequantize(self.codes[i], self.scales[i], self.n, zq.INT8, self.G, out=self.out[i])
+        # The calls are independent, so each graph forks into `streams` chains
+        # (call i on chain i % streams) that join at its end; the GPU runs the
+        # chains concurrently, each chain's calls in order.
+        side = [torch.cuda.Stream() for _ in range(self.streams)]
+
+        def capture(graph, call):
+            with torch.cuda.graph(graph, stream=s):
+                for st in side:
+                    st.wait_stream(s)
+                for i in range(self.copies):
+                    with torch.cuda.stream(side[i % self.streams]):
+                        call(i)
+                for st in side:
+                    s.wait_stream(st)
+
+        capture(self.gq, lambda i: zq.quantize(self.src[i], zq.INT8, self.G, self.codes[i],
+                                               self.scales[i]))
+        capture(self.gd, lambda i: zq.dequantize(self.codes[i], self.scales[i], self.n, zq.INT8,
+                                                 self.G, out=self.out[i]))
         torch.cuda.synchronize()
 
     def launches(self):
@@ -376,6 +393,7 @@ class QgzReduce:
     reduces them to int4 G=128 and, separately, to int8 G=256."""
 
     name = "qgz_reduce"
+    dtype = "int4 codes + fp32 scales in, fp32 sums, int4/int8 codes out"
     N = 8
     n = 134217728
 
@@ -467,6 +485,7 @@ class AgoqFP8:
     peer sends after the all-to-all)."""
 
     name = "agoq_fp8"
+    dtype = "e4m3 codes + fp32 scales, bf16 gradients in, fp32 sums"
     n = 268435456
     G = 128
     steps = 4
@@ -575,6 +594,7 @@ class Llama70B:
     dequantize -> bf16, one call per matrix."""
 
     name = "llama70b"
+    dtype = "bf16 in, int8 / int6 codes + fp32 scales, bf16 out (fp32 arithmetic)"
     schemes = ((8, 256), (6, 32))
 
     def config(self):
@@ -777,7 +797,7 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": wl.config(),
+            "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic", "config": wl.config(),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -894,7 +914,7 @@ def run_gpu(args, rank, world, local):
     line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(elapsed_max / args.steps * 1e3, 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16->int2/4/6/8 (fp32 scale math)",
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
             "data": "synthetic (seeded, blockwise_quantized_zero_gb300.inputs)",
             "config": dict(wl.config(), parallelism=f"replicas x{world} (no collective)"),
             "frac_of_peak": round(value / peak, 4),
