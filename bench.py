@@ -139,6 +139,33 @@ class Launch:
         self.kernels = kernels
 
 
+class ForkedStreams:
+    """Two side streams forked from the current stream and joined back to it,
+    for end-to-end steps whose items are independent: item k runs on side
+    stream k % 2 with buffer set k % 2, so one item's device-to-host copies
+    overlap the next item's host-to-device copies (the host link is full
+    duplex). Each stream reuses its buffer set only after its own previous
+    item, in stream order."""
+
+    def __init__(self, make_set):
+        import torch
+
+        self.streams = [torch.cuda.Stream() for _ in range(2)]
+        self.sets = [make_set() for _ in range(2)]
+
+    def run(self, items, fn):
+        import torch
+
+        cur = torch.cuda.current_stream()
+        for st in self.streams:
+            st.wait_stream(cur)
+        for k, item in enumerate(items):
+            with torch.cuda.stream(self.streams[k % 2]):
+                fn(item, self.sets[k % 2])
+        for st in self.streams:
+            cur.wait_stream(st)
+
+
 def _dev_bf16(bits: np.ndarray):
     import torch
 
@@ -203,39 +230,49 @@ class GMSweep:
     def setup_e2e(self):
         import torch
 
-        zq = self.zq
+        zq, n = self.zq, self.n
         self.h_src = torch.from_numpy(self.host.view(np.int16)).view(torch.bfloat16).pin_memory()
-        cmax = max(zq.codes_bytes(b, self.n) for b in self.bits)
-        smax = zq.num_blocks(self.n, 32)
-        self.h_codes = torch.empty(cmax, dtype=torch.uint8).pin_memory()
-        self.h_scales = torch.empty(smax, dtype=torch.float32).pin_memory()
-        self.h_out = torch.empty(self.n, dtype=torch.bfloat16).pin_memory()
-        self.d_src = torch.empty(self.n, dtype=torch.bfloat16, device="cuda")
-        self.d_codes = torch.empty(cmax, dtype=torch.uint8, device="cuda")
-        self.d_scales = torch.empty(smax, dtype=torch.float32, device="cuda")
-        self.d_codes2 = torch.empty(cmax, dtype=torch.uint8, device="cuda")
-        self.d_scales2 = torch.empty(smax, dtype=torch.float32, device="cuda")
-        self.d_out = torch.empty(self.n, dtype=torch.bfloat16, device="cuda")
+        cmax = max(zq.codes_bytes(b, n) for b in self.bits)
+        smax = zq.num_blocks(n, 32)
+
+        def make_set():
+            dev = dict(device="cuda")
+            return dict(h_codes=torch.empty(cmax, dtype=torch.uint8).pin_memory(),
+                        h_scales=torch.empty(smax, dtype=torch.float32).pin_memory(),
+                        h_out=torch.empty(n, dtype=torch.bfloat16).pin_memory(),
+                        d_src=torch.empty(n, dtype=torch.bfloat16, **dev),
+                        d_codes=torch.empty(cmax, dtype=torch.uint8, **dev),
+                        d_scales=torch.empty(smax, dtype=torch.float32, **dev),
+                        d_codes2=torch.empty(cmax, dtype=torch.uint8, **dev),
+                        d_scales2=torch.empty(smax, dtype=torch.float32, **dev),
+                        d_out=torch.empty(n, dtype=torch.bfloat16, **dev))
+
+        self.fork = ForkedStreams(make_set)
         h2d = d2h = 0
         for b, G in self.pairs:
-            cb, sb = self.zq.codes_bytes(b, self.n), 4 * self.zq.num_blocks(self.n, G)
-            h2d += 2 * self.n + cb + sb
-            d2h += cb + sb + 2 * self.n
+            cb, sb = self.zq.codes_bytes(b, n), 4 * self.zq.num_blocks(n, G)
+            h2d += 2 * n + cb + sb
+            d2h += cb + sb + 2 * n
         return h2d, d2h
 
     def e2e_step(self):
-        """Per pair: host src -> quantize -> host codes; host codes -> dequantize -> host out."""
+        """Per pair: host src -> quantize -> host codes; host codes -> dequantize
+        -> host out. Pairs alternate between two streams (ForkedStreams)."""
         zq, n = self.zq, self.n
-        for b, G in self.pairs:
+
+        def one(pair, B):
+            b, G = pair
             cb, nb = zq.codes_bytes(b, n), zq.num_blocks(n, G)
-            self.d_src.copy_(self.h_src, non_blocking=True)
-            zq.quantize(self.d_src, b, G, self.d_codes[:cb], self.d_scales[:nb])
-            self.h_codes[:cb].copy_(self.d_codes[:cb], non_blocking=True)
-            self.h_scales[:nb].copy_(self.d_scales[:nb], non_blocking=True)
-            self.d_codes2[:cb].copy_(self.h_codes[:cb], non_blocking=True)
-            self.d_scales2[:nb].copy_(self.h_scales[:nb], non_blocking=True)
-            zq.dequantize(self.d_codes2[:cb], self.d_scales2[:nb], n, b, G, out=self.d_out)
-            self.h_out.copy_(self.d_out, non_blocking=True)
+            B["d_src"].copy_(self.h_src, non_blocking=True)
+            zq.quantize(B["d_src"], b, G, B["d_codes"][:cb], B["d_scales"][:nb])
+            B["h_codes"][:cb].copy_(B["d_codes"][:cb], non_blocking=True)
+            B["h_scales"][:nb].copy_(B["d_scales"][:nb], non_blocking=True)
+            B["d_codes2"][:cb].copy_(B["h_codes"][:cb], non_blocking=True)
+            B["d_scales2"][:nb].copy_(B["h_scales"][:nb], non_blocking=True)
+            zq.dequantize(B["d_codes2"][:cb], B["d_scales2"][:nb], n, b, G, out=B["d_out"])
+            B["h_out"].copy_(B["d_out"], non_blocking=True)
+
+        self.fork.run(self.pairs, one)
 
     def step_bytes(self):
         return sum(2 * (2 * self.n + packed_bytes(b, self.n, G)) for b, G in self.pairs)
@@ -347,23 +384,29 @@ class QwzFP16:
         zq, n = self.zq, self.n
         self.e_copies = 64
         self.h_src = torch.from_numpy(self.host).pin_memory()
-        self.h_codes = torch.empty(zq.codes_bytes(zq.INT8, n), dtype=torch.uint8).pin_memory()
-        self.h_scales = torch.empty(zq.num_blocks(n, self.G), dtype=torch.float32).pin_memory()
-        self.h_out = torch.empty(n, dtype=torch.float32).pin_memory()
+        self.fork = ForkedStreams(lambda: dict(
+            h_codes=torch.empty(zq.codes_bytes(zq.INT8, n), dtype=torch.uint8).pin_memory(),
+            h_scales=torch.empty(zq.num_blocks(n, self.G), dtype=torch.float32).pin_memory(),
+            h_out=torch.empty(n, dtype=torch.float32).pin_memory()))
         pb = packed_bytes(8, n, self.G)
         return self.e_copies * (2 * n + pb), self.e_copies * (pb + 4 * n)
 
     def e2e_step(self):
+        """64 calls, each from host memory to host memory; the calls alternate
+        between two streams (ForkedStreams)."""
         zq, n = self.zq, self.n
-        for i in range(self.e_copies):
+
+        def one(i, B):
             self.src[i].copy_(self.h_src, non_blocking=True)
             zq.quantize(self.src[i], zq.INT8, self.G, self.codes[i], self.scales[i])
-            self.h_codes.copy_(self.codes[i], non_blocking=True)
-            self.h_scales.copy_(self.scales[i], non_blocking=True)
-            self.codes[i].copy_(self.h_codes, non_blocking=True)
-            self.scales[i].copy_(self.h_scales, non_blocking=True)
+            B["h_codes"].copy_(self.codes[i], non_blocking=True)
+            B["h_scales"].copy_(self.scales[i], non_blocking=True)
+            self.codes[i].copy_(B["h_codes"], non_blocking=True)
+            self.scales[i].copy_(B["h_scales"], non_blocking=True)
             zq.dequantize(self.codes[i], self.scales[i], n, zq.INT8, self.G, out=self.out[i])
-            self.h_out.copy_(self.out[i], non_blocking=True)
+            B["h_out"].copy_(self.out[i], non_blocking=True)
+
+        self.fork.run(range(self.e_copies), one)
 
     def e2e_bytes(self):
         pb = packed_bytes(8, self.n, self.G)
@@ -643,7 +686,9 @@ class Llama70B:
         import torch
 
         name, n, x = self.mats[4]  # gate, 8192 x 28672
+        assert n % (4 * 1024) == 0
         self.e_name, self.e_n = name, n
+        self.fork = ForkedStreams(dict)
         self.h_x = x.cpu().pin_memory()
         self.h_c = torch.empty(n, dtype=torch.uint8).pin_memory()
         self.h_s = torch.empty(n // 32, dtype=torch.float32).pin_memory()
@@ -656,19 +701,32 @@ class Llama70B:
         return h2d, d2h
 
     def e2e_step(self):
-        """The gate matrix from host memory through both schemes, results to host."""
+        """The gate matrix from host memory through both schemes, results to
+        host, in four row chunks per scheme (chunk boundaries are block
+        boundaries, so the results are those of whole-matrix calls). Items
+        alternate between two streams (ForkedStreams); with four chunks per
+        scheme a chunk's two items share a stream, so no slice is touched by
+        both streams."""
         zq, n = self.zq, self.e_n
         x = self.mats[4][2]
-        for b, G in self.schemes:
+        q = n // 4
+        items = [(b, G, j) for b, G in self.schemes for j in range(4)]
+
+        def one(item, _):
+            b, G, j = item
             c, s, y = self.buf[(b, G, self.e_name)]
-            x.copy_(self.h_x, non_blocking=True)
-            zq.quantize(x, b, G, c, s)
-            self.h_c[: c.numel()].copy_(c, non_blocking=True)
-            self.h_s[: s.numel()].copy_(s, non_blocking=True)
-            c.copy_(self.h_c[: c.numel()], non_blocking=True)
-            s.copy_(self.h_s[: s.numel()], non_blocking=True)
-            zq.dequantize(c, s, n, b, G, out=y)
-            self.h_y.copy_(y, non_blocking=True)
+            lo, hi = j * q, (j + 1) * q
+            clo, chi = lo * b // 8, hi * b // 8
+            x[lo:hi].copy_(self.h_x[lo:hi], non_blocking=True)
+            zq.quantize(x[lo:hi], b, G, c[clo:chi], s[lo // G:hi // G])
+            self.h_c[clo:chi].copy_(c[clo:chi], non_blocking=True)
+            self.h_s[lo // G:hi // G].copy_(s[lo // G:hi // G], non_blocking=True)
+            c[clo:chi].copy_(self.h_c[clo:chi], non_blocking=True)
+            s[lo // G:hi // G].copy_(self.h_s[lo // G:hi // G], non_blocking=True)
+            zq.dequantize(c[clo:chi], s[lo // G:hi // G], hi - lo, b, G, out=y[lo:hi])
+            self.h_y[lo:hi].copy_(y[lo:hi], non_blocking=True)
+
+        self.fork.run(items, one)
 
     def e2e_bytes(self):
         n = self.e_n
@@ -840,13 +898,32 @@ def run_gpu(args, rank, world, local):
         step()
     torch.cuda.synchronize()
 
-    # Two timed regions of K steps each. The first runs the launches back to
+    # Three timed regions of K steps each. The first runs the launches back to
     # back, as a user's stream does (the kernels use programmatic dependent
     # launch, which an event recorded between two launches would defeat): it
-    # gives `value`. The second brackets every launch with an event pair: it
-    # gives each kernel's own duration for the roofline.
+    # gives `value`. The second records events only where the kernel family
+    # changes, so each family's launches still run back to back: its group
+    # times give each family's average launch duration for the roofline. The
+    # third brackets every launch with an event pair, for the per-launch table
+    # (isolated launches, so it includes each launch's start-up).
+    groups = []  # maximal runs of consecutive launches of one family
+    for i, l in enumerate(launches):
+        if groups and groups[-1][0] == l.family:
+            groups[-1][1].append(i)
+        else:
+            groups.append((l.family, [i]))
+    gevs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in groups] for _ in range(args.steps)]
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in launches] for _ in range(args.steps)]
+
+    def step_groups(gev):
+        for gi, (_, idx) in enumerate(groups):
+            gev[gi][0].record(stream)
+            for i in idx:
+                launches[i].fn()
+            gev[gi][1].record(stream)
+
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         barrier(world)
@@ -858,6 +935,10 @@ def run_gpu(args, rank, world, local):
         torch.cuda.synchronize()
         barrier(world)
         for k in range(args.steps):
+            step_groups(gevs[k])
+        torch.cuda.synchronize()
+        barrier(world)
+        for k in range(args.steps):
             step(evs[k])
         torch.cuda.synchronize()
         barrier(world)
@@ -865,16 +946,19 @@ def run_gpu(args, rank, world, local):
     elapsed_max = max_over_ranks(elapsed, world)
     value, _ = aggregate(step_bytes * args.steps, [elapsed_max], world)
 
-    # per-kernel-family launch durations
+    # per-kernel-family durations (launches of a family back to back)
     fam = {}
+    for k in range(args.steps):
+        for gi, (family, idx) in enumerate(groups):
+            f = fam.setdefault(family, [0.0, 0, 0])
+            f[0] += gevs[k][gi][0].elapsed_time(gevs[k][gi][1])
+            f[1] += sum(launches[i].nbytes for i in idx)
+            f[2] += sum(launches[i].kernels for i in idx)
+    # per-launch durations (each launch bracketed by events)
     per_label = {}
     for k in range(args.steps):
         for i, l in enumerate(launches):
             ms = evs[k][i][0].elapsed_time(evs[k][i][1])
-            f = fam.setdefault(l.family, [0.0, 0, 0])
-            f[0] += ms
-            f[1] += l.nbytes
-            f[2] += 1
             pl = per_label.setdefault(l.label, [0.0, 0, 0])
             pl[0] += ms
             pl[1] += l.nbytes
@@ -882,7 +966,6 @@ def run_gpu(args, rank, world, local):
     dominant = max(fam, key=lambda k: fam[k][0])
     peak, peak_src = measured_peak()
     ms_sum, nbytes, count = fam[dominant]
-    count = sum(l.kernels for l in launches if l.family == dominant) * args.steps
     achieved = nbytes / (ms_sum / 1e3) / 1e9
     traffic = lookup_traffic(dominant)
     kpl = {l.label: l.kernels for l in launches}
@@ -928,8 +1011,13 @@ def run_gpu(args, rank, world, local):
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": sum(l.kernels for l in launches) * args.steps,
-            "gpu_launches_note": "per timed region; a second region of as many launches, "
-                                 "each bracketed by events, times the kernels one by one",
+            "gpu_launches_note": "per timed region (the value's); two more regions of as many "
+                                 "launches time the kernel families (events only between "
+                                 "families) and each launch alone (the kernels table)",
+            "families": {k: {"gbs": round(v[1] / (v[0] / 1e3) / 1e9, 1),
+                             "frac": round(v[1] / (v[0] / 1e3) / 1e9 / peak, 4),
+                             "us_per_launch": round(v[0] / v[2] * 1e3, 2), "launches": v[2]}
+                         for k, v in fam.items()},
             "clocks": clocks.summary()}
     return line
 
