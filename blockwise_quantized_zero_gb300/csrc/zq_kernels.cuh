@@ -259,6 +259,10 @@ __global__ void __launch_bounds__(kThreads, 3) quantize_kernel(const void *__res
 // ===========================================================================
 // Dequantize
 // ===========================================================================
+// Tiles in flight per warp: 6 for codes of up to 4 bits, 4 for wider codes
+// (whose larger register slots would otherwise cost occupancy).
+template <int FMT> constexpr int kDequantAhead = Fmt<FMT>::kBits <= 4 ? 6 : 4;
+
 template <int FMT, int DT>
 __global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t *__restrict__ codes,
                                                               const float *__restrict__ scales,
@@ -268,35 +272,45 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t *__r
   const WarpCursor c;
   const int64_t nfull = n / kTile;
   const bool wd = wide != 0;
-  // Software pipeline: codes and scales of tile t + nwarps are loaded while
-  // tile t is decoded and stored.
-  uint32_t w[kU][W];
-  float s[kU];
-  int64_t t = c.warp;
-  auto load = [&](int64_t tile) {
+  // Software pipeline: the codes and scales of the warp's next PF tiles are
+  // in flight (a ring of register slots) while tile t is decoded and
+  // stored; the loads are small, so several are needed to cover the latency.
+  constexpr int PF = kDequantAhead<FMT>;
+  uint32_t w[PF][kU][W];
+  float s[PF][kU];
+  auto load = [&](int64_t tile, uint32_t (&wd_)[kU][W], float (&sd_)[kU]) {
 #pragma unroll
     for (int j = 0; j < kU; ++j) {
       const int64_t e = tile * kTile + j * kRun + c.lane * kVec;
-      load_codes16<B>(codes + e * B / 8, w[j]);
-      s[j] = ld_nc_f32(scales + (e >> log2G));
+      load_codes16<B>(codes + e * B / 8, wd_[j]);
+      sd_[j] = ld_nc_f32(scales + (e >> log2G));
     }
   };
-  if (t < nfull) load(t);
-  for (; t < nfull; t += c.nwarps) {
-    uint32_t wc[kU][W];
-    float sc[kU];
 #pragma unroll
-    for (int j = 0; j < kU; ++j) {
-      sc[j] = s[j];
+  for (int k = 0; k < PF; ++k)
+    if (c.warp + k * c.nwarps < nfull) load(c.warp + k * c.nwarps, w[k], s[k]);
+  for (int64_t t = c.warp; t < nfull;) {
 #pragma unroll
-      for (int k = 0; k < W; ++k) wc[j][k] = w[j][k];
-    }
-    if (t + c.nwarps < nfull) load(t + c.nwarps);
+    for (int k = 0; k < PF; ++k) {  // slot k holds tile t
+      if (t < nfull) {
+        uint32_t wc[kU][W];
+        float sc[kU];
 #pragma unroll
-    for (int j = 0; j < kU; ++j) {
-      float y[kVec];
-      dequant16<FMT>(wc[j], sc[j], y);
-      store16<DT>(dst, t * kTile + j * kRun + c.lane * kVec, y, wd);
+        for (int j = 0; j < kU; ++j) {
+          sc[j] = s[k][j];
+#pragma unroll
+          for (int q = 0; q < W; ++q) wc[j][q] = w[k][j][q];
+        }
+        const int64_t tn = t + PF * c.nwarps;
+        if (tn < nfull) load(tn, w[k], s[k]);
+#pragma unroll
+        for (int j = 0; j < kU; ++j) {
+          float y[kVec];
+          dequant16<FMT>(wc[j], sc[j], y);
+          store16<DT>(dst, t * kTile + j * kRun + c.lane * kVec, y, wd);
+        }
+        t += c.nwarps;
+      }
     }
   }
   if (c.owns_tail(n)) {
