@@ -967,7 +967,7 @@ def run_gpu(args, rank, world, local):
     peak, peak_src = measured_peak()
     ms_sum, nbytes, count = fam[dominant]
     achieved = nbytes / (ms_sum / 1e3) / 1e9
-    traffic = lookup_traffic(dominant)
+    traffic = lookup_traffic(wl.name, dominant)
     kpl = {l.label: l.kernels for l in launches}
     kernels = {k: {"gbs": round(v[1] / (v[0] / 1e3) / 1e9, 1),
                    "frac": round(v[1] / (v[0] / 1e3) / 1e9 / peak, 3),
@@ -1022,9 +1022,10 @@ def run_gpu(args, rank, world, local):
     return line
 
 
-def lookup_traffic(family: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources; None otherwise."""
+def lookup_traffic(workload: str, family: str):
+    """DRAM bytes per launch of a workload's kernel family from the committed
+    ncu summaries, if they were taken on the current kernel sources; None
+    otherwise."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -1033,7 +1034,7 @@ def lookup_traffic(family: str):
         return None
     if d.get("csrc_sha") != csrc_sha():
         return None
-    return d.get("families", {}).get(family)
+    return d.get("workloads", {}).get(workload, {}).get(family)
 
 
 def csrc_sha() -> str:
