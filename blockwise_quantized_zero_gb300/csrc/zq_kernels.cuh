@@ -370,15 +370,21 @@ struct TableReduceArgs {
 // packed fma of the rounded product with `one`, a 1.0f that arrives at run
 // time: fl(d * 1 + acc) = fl(d + acc) exactly, and since ptxas cannot know
 // that `one` is 1, it can neither drop the multiply nor fold the product in.
-template <int FIN>
+// FIRST: acc = fl(+0 + d) for the first shard (the sum starts at +0; the
+// addend is the constant 0, so the registers need no clearing).
+template <int FIN, bool FIRST = false>
 __device__ __forceinline__ void accumulate16(float (&acc)[kVec],
                                              const uint32_t (&w)[Fmt<FIN>::kWords16], float s,
                                              float one) {
   float d[kVec];
   dequant16<FIN>(w, s, d);
 #pragma unroll
-  for (int v = 0; v < kVec; v += 2)
-    fma2(acc[v], acc[v + 1], d[v], d[v + 1], one, one, acc[v], acc[v + 1]);
+  for (int v = 0; v < kVec; v += 2) {
+    if constexpr (FIRST)
+      fma2(acc[v], acc[v + 1], d[v], d[v + 1], one, one, 0.0f, 0.0f);
+    else
+      fma2(acc[v], acc[v + 1], d[v], d[v + 1], one, one, acc[v], acc[v + 1]);
+  }
 }
 
 // Requantize the sums of one tile of KU runs (KU*512 elements) with block
@@ -508,14 +514,18 @@ __device__ __forceinline__ void load_codes16_smem(const uint8_t *p, uint32_t (&w
 constexpr int kRedConsumers = 8;
 constexpr int kRedThreads = (kRedConsumers + 1) * 32;
 
+// Stage geometry (measured): 2-bit codes use four stages of up to 24 KB, wider
+// codes two stages of up to 40 KB (more shards per unit, fewer unit
+// overheads); two CTAs of 9 warps fit on an SM either way.
 template <int FIN> struct RedGeom {
   static constexpr int kCodeBytes = kTile * Fmt<FIN>::kBits / 8;  // one shard, one tile
   static constexpr int kShardBytes =                               // codes + room for G_in = 32
       kRedConsumers * kCodeBytes + kRedConsumers * (kTile / 32) * 4;
-  static constexpr int kShards = (24576 / kShardBytes) > 1 ? 24576 / kShardBytes : 1;
+  static constexpr int kBudget = Fmt<FIN>::kBits <= 2 ? 24576 : 40960;
+  static constexpr int kShards = (kBudget / kShardBytes) > 1 ? kBudget / kShardBytes : 1;
   static constexpr int kScaleOff = kShards * kRedConsumers * kCodeBytes;
   static constexpr int kStage = kShards * kShardBytes;
-  static constexpr int kStages = 4;
+  static constexpr int kStages = Fmt<FIN>::kBits <= 2 ? 4 : 2;
   static constexpr int kBarOff = kStages * kStage;
   static constexpr int kSmem = kBarOff + kStages * 16;  // full + empty barrier per stage
   static_assert(kCodeBytes % 16 == 0 && kStage % 16 == 0, "bulk copies need 16-byte multiples");
@@ -607,42 +617,36 @@ __global__ void __launch_bounds__(kRedThreads, 2)
     const int cnt = int(left < kRedConsumers ? left : kRedConsumers);
     const bool stma = ((cnt * nbt * 4) % 16) == 0;
     const int64_t e0 = (ct * kRedConsumers + w) * kTile;
-    if (k == 0) {
-#pragma unroll
-      for (int j = 0; j < kU; ++j)
-#pragma unroll
-        for (int v = 0; v < kVec; ++v) acc[j][v] = 0.0f;
-    }
     if (w < cnt) {
       const uint8_t *sb = red_smem + st * RG::kStage;
-      if (stma) {  // scales in the stage
+      // shard q of the unit: codes from the stage, scale from the stage or
+      // from global memory (G_in >= 512 at the end of the tensor); the first
+      // shard of a tile starts the sum
+      auto shard = [&](int q, auto first, auto scales_in_stage) {
+        const uint8_t *cq = sb + (q * kRedConsumers + w) * CB;
+        const float *sq =
+            reinterpret_cast<const float *>(sb + RG::kScaleOff) + (q * kRedConsumers + w) * nbt;
 #pragma unroll
-        for (int q = 0; q < RG::kShards; ++q) {
-          if (q < ns) {  // shard order is the summation order
-            const uint8_t *cq = sb + (q * kRedConsumers + w) * CB;
-            const float *sq = reinterpret_cast<const float *>(sb + RG::kScaleOff) +
-                              (q * kRedConsumers + w) * nbt;
-#pragma unroll
-            for (int j = 0; j < kU; ++j) {
-              const int off = j * kRun + lane * kVec;
-              uint32_t wv[WIN];
-              load_codes16_smem<BIN>(cq + off * BIN / 8, wv);
-              accumulate16<FIN>(acc[j], wv, sq[off >> lgin], a.one);
-            }
-          }
+        for (int j = 0; j < kU; ++j) {
+          const int off = j * kRun + lane * kVec;
+          uint32_t wv[WIN];
+          load_codes16_smem<BIN>(cq + off * BIN / 8, wv);
+          const float s = decltype(scales_in_stage)::value
+                              ? sq[off >> lgin]
+                              : ld_nc_f32(a.shard_scales(r0 + q) + ((e0 + off) >> lgin));
+          accumulate16<FIN, decltype(first)::value>(acc[j], wv, s, a.one);
         }
-      } else {  // scales from global memory (G_in >= 512 at the end of the tensor)
-        for (int q = 0; q < ns; ++q) {
-          const uint8_t *cq = sb + (q * kRedConsumers + w) * CB;
-          const float *sg = a.shard_scales(r0 + q);
+      };
+      using T = std::true_type;
+      using F = std::false_type;
+      if (stma) {
+        if (k == 0) shard(0, T{}, T{}); else shard(0, F{}, T{});
 #pragma unroll
-          for (int j = 0; j < kU; ++j) {
-            const int off = j * kRun + lane * kVec;
-            uint32_t wv[WIN];
-            load_codes16_smem<BIN>(cq + off * BIN / 8, wv);
-            accumulate16<FIN>(acc[j], wv, ld_nc_f32(sg + ((e0 + off) >> lgin)), a.one);
-          }
-        }
+        for (int q = 1; q < RG::kShards; ++q)
+          if (q < ns) shard(q, F{}, T{});  // shard order is the summation order
+      } else {
+        if (k == 0) shard(0, T{}, F{}); else shard(0, F{}, F{});
+        for (int q = 1; q < ns; ++q) shard(q, F{}, F{});
       }
     }
     __syncwarp();  // every lane has read the stage
