@@ -68,6 +68,9 @@ def _declare(lib):
     lib.orc_dequantize.argtypes = [vp, vp, i64, i32, i64, vp, i32]
     lib.orc_reduce.argtypes = [vp, vp, i32, i64, i32, i64, vp, vp, i32, i64, vp]
     lib.orc_fp8_accumulate.argtypes = [vp, vp, vp, i32, i64, i64]
+    lib.orc_quantize_reordered.argtypes = [vp, i32, i64, i32, i64, i32, i32, vp, vp]
+    lib.orc_reduce_two_hop.argtypes = [vp, vp, i32, i32, i64, i32, i64, vp, vp, i32, i64, vp, vp,
+                                       i32, i64, vp]
     lib.orc_encode_n.argtypes = [i32, vp, i64, vp]
     lib.orc_decode_n.argtypes = [i32, vp, i64, vp]
     lib.orc_encode_n.restype = i32
@@ -165,6 +168,63 @@ def reduce(codes_list, scales_list, n: int, fmt_in: int, G_in: int, fmt_out: int
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return out_codes, out_scales, sum_out
+
+
+def slice_position(c: int, A: int, L: int) -> int:
+    """Where chunk c sits in the reordered layout (the transpose of the A x L grid)."""
+    return (c % L) * A + c // L
+
+
+def quantize_reordered(x: np.ndarray, fmt: int, G: int, A: int, L: int, dtype: int | None = None,
+                       lib=None):
+    """Quantize with tensor-slice reordering: (codes, scales) of the whole tensor,
+    chunk c of n/(A*L) elements stored at slice position slice_position(c)."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x)
+    n = x.size
+    codes = np.full(codes_bytes(fmt, n, lib), GARBAGE, dtype=np.uint8)
+    scales = np.full(max(num_blocks(n, G, lib), 0), np.nan, dtype=np.float32)
+    rc = lib.orc_quantize_reordered(_ptr(x), _dtype_code(x, dtype), n, fmt, G, A, L, _ptr(codes),
+                                    _ptr(scales))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return codes, scales
+
+
+def reduce_two_hop(codes_list, scales_list, A: int, L: int, n: int, fmt_in: int, G_in: int,
+                   fmt_mid: int, G_mid: int, fmt_out: int, G_out: int, want_sum: bool = False,
+                   lib=None):
+    """Two-hop reduce over P = A*L simulated GPUs. Returns (mid, out, sums): mid and
+    out are lists of (codes, scales) per GPU (A*n/P and n/P elements), sums a list
+    of fp32 arrays (or None)."""
+    lib = lib or load()
+    P = A * L
+    if len(codes_list) != P or len(scales_list) != P:
+        raise ValueError("need one codes and one scales array per GPU")
+    m = n // P
+    codes_list = [np.ascontiguousarray(c, dtype=np.uint8) for c in codes_list]
+    scales_list = [np.ascontiguousarray(s, dtype=np.float32) for s in scales_list]
+    mid = [(np.full(codes_bytes(fmt_mid, A * m, lib), GARBAGE, np.uint8),
+            np.full(num_blocks(A * m, G_mid, lib), np.nan, np.float32)) for _ in range(P)]
+    out = [(np.full(codes_bytes(fmt_out, m, lib), GARBAGE, np.uint8),
+            np.full(num_blocks(m, G_out, lib), np.nan, np.float32)) for _ in range(P)]
+    sums = [np.full(m, np.nan, np.float32) for _ in range(P)] if want_sum else None
+
+    def arr(items):
+        return (ctypes.c_void_p * P)(*[_ptr(a) for a in items])
+
+    # every pointer array is bound to a name so that it outlives the call
+    ic, is_ = arr(codes_list), arr(scales_list)
+    mc, ms = arr([c for c, _ in mid]), arr([s for _, s in mid])
+    oc, os_ = arr([c for c, _ in out]), arr([s for _, s in out])
+    sp = arr(sums) if want_sum else None
+    rc = lib.orc_reduce_two_hop(
+        ctypes.addressof(ic), ctypes.addressof(is_), A, L, n, fmt_in, G_in, ctypes.addressof(mc),
+        ctypes.addressof(ms), fmt_mid, G_mid, ctypes.addressof(oc), ctypes.addressof(os_), fmt_out,
+        G_out, ctypes.addressof(sp) if want_sum else None)
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return mid, out, sums
 
 
 def fp8_accumulate(codes: np.ndarray, scales: np.ndarray, grad: np.ndarray, G: int,

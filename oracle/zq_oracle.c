@@ -47,6 +47,25 @@
  *  R8  the FP8 accumulate adds in fp32: v = fl(fl(D8(c) * s) + g);
  *  R9  a block whose scale is zero (all-zero block, or a scale that
  *      underflows to zero) gets all-zero code bits.
+ *  R10 qgZ's hierarchy ([ZeRO++] sections "Two-hop communication prevents
+ *      QGZ traffic from multiplying across GPUs" and "Tensor-slice
+ *      reordering fixes incorrect gradient placement"): P = A*L GPUs, A
+ *      nodes of L GPUs, GPU g = a*L + l; every gradient is split into P equal
+ *      chunks and chunk c is the one GPU c owns after the reduce-scatter.
+ *      The reordering is the transpose of the A x L chunk grid: chunk
+ *      c = a*L + l is stored at slice position l*A + a, so that part l
+ *      (positions l*A .. l*A+A-1) holds, node by node, the chunks that local
+ *      GPU l of every node will own. (The pages show an example swap, not a
+ *      rule; this is the permutation that makes the two hops below deliver
+ *      chunk g to GPU g.)
+ *  R11 hop 1 (intra-node, the fused "dequantization and reduction with
+ *      inter-node quantization"): GPU (a, l) sums part l of GPUs
+ *      (a, 0), ..., (a, L-1) in that order and requantizes it; hop 2
+ *      (inter-node): GPU (a, l) sums the a-th chunk of the hop-1 results of
+ *      GPUs (0, l), ..., (A-1, l) in that order and requantizes it. Each hop
+ *      is one reduce as in R7.
+ *  R12 the chunk size n / P is a multiple of 1024 elements, so every chunk
+ *      is whole blocks and whole code words.
  */
 #include <math.h>
 #include <stddef.h>
@@ -380,6 +399,82 @@ int orc_reduce(const uint8_t *const *codes, const float *const *scales, int nsha
         }
         out_scales[k] = quantize_block(scratch, len, fmt_out, out_codes, lo);
     }
+    return ORC_OK;
+}
+
+/* Slice position of chunk c (reading R10). */
+static int64_t slice_position(int64_t c, int A, int L) { return (c % L) * A + c / L; }
+
+static int two_hop_ok(int64_t n, int A, int L)
+{
+    int64_t P = (int64_t)A * L;
+    return A >= 1 && L >= 1 && A <= 64 && L <= 64 && n >= 0 && n % (P * 1024) == 0;
+}
+
+/* Quantize with tensor-slice reordering ([ZeRO++] "Tensor-slice reordering
+ * fixes incorrect gradient placement", readings R10 and R12): the n elements
+ * form P = A*L chunks of m = n/P; chunk c is quantized on its own and its
+ * codes and scales are written at slice position (c % L)*A + c/L. */
+int orc_quantize_reordered(const void *src, int dtype, int64_t n, int fmt, int64_t G, int A, int L,
+                           uint8_t *codes, float *scales)
+{
+    int64_t P, m, c;
+    if (!code_bits(fmt) || !valid_block(G) || !elem_size(dtype) || !two_hop_ok(n, A, L))
+        return ORC_BAD;
+    P = (int64_t)A * L;
+    m = n / P;
+    for (c = 0; c < P; ++c) {
+        int64_t pos = slice_position(c, A, L);
+        int rc = orc_quantize((const char *)src + c * m * elem_size(dtype), dtype, m, fmt, G,
+                              codes + pos * m * code_bits(fmt) / 8, scales + pos * m / G);
+        if (rc != ORC_OK) return rc;
+    }
+    return ORC_OK;
+}
+
+/* Two-hop quantized reduce (readings R10-R12), all GPUs simulated here.
+ * codes[g], scales[g]: GPU g's n elements in the reordered layout (fmt_in,
+ * G_in). Hop 1: mid[a*L + l] = requant_(fmt_mid, G_mid)( sum over l2 = 0..L-1
+ * of part l of GPU a*L + l2 ), A*m elements. Hop 2: out[a*L + l] =
+ * requant_(fmt_out, G_out)( sum over a2 = 0..A-1 of chunk a of mid[a2*L + l] ),
+ * m elements: the reduced chunk a*L + l. sums[g] (optional, m floats each)
+ * receives hop 2's fp32 sums. */
+int orc_reduce_two_hop(const uint8_t *const *codes, const float *const *scales, int A, int L,
+                       int64_t n, int fmt_in, int64_t G_in, uint8_t *const *mid_codes,
+                       float *const *mid_scales, int fmt_mid, int64_t G_mid,
+                       uint8_t *const *out_codes, float *const *out_scales, int fmt_out,
+                       int64_t G_out, float *const *sums)
+{
+    const uint8_t *sc[64];
+    const float *ss[64];
+    int64_t m;
+    int a, l, r, rc;
+    if (!code_bits(fmt_in) || !code_bits(fmt_mid) || !code_bits(fmt_out) || !valid_block(G_in) ||
+        !valid_block(G_mid) || !valid_block(G_out) || !two_hop_ok(n, A, L))
+        return ORC_BAD;
+    m = n / ((int64_t)A * L);
+    for (a = 0; a < A; ++a)      /* hop 1 */
+        for (l = 0; l < L; ++l) {
+            int64_t off = (int64_t)l * A * m;
+            for (r = 0; r < L; ++r) {
+                sc[r] = codes[a * L + r] + off * code_bits(fmt_in) / 8;
+                ss[r] = scales[a * L + r] + off / G_in;
+            }
+            rc = orc_reduce(sc, ss, L, (int64_t)A * m, fmt_in, G_in, mid_codes[a * L + l],
+                            mid_scales[a * L + l], fmt_mid, G_mid, 0);
+            if (rc != ORC_OK) return rc;
+        }
+    for (a = 0; a < A; ++a)      /* hop 2 */
+        for (l = 0; l < L; ++l) {
+            int64_t off = (int64_t)a * m;
+            for (r = 0; r < A; ++r) {
+                sc[r] = mid_codes[r * L + l] + off * code_bits(fmt_mid) / 8;
+                ss[r] = mid_scales[r * L + l] + off / G_mid;
+            }
+            rc = orc_reduce(sc, ss, A, m, fmt_mid, G_mid, out_codes[a * L + l],
+                            out_scales[a * L + l], fmt_out, G_out, sums ? sums[a * L + l] : 0);
+            if (rc != ORC_OK) return rc;
+        }
     return ORC_OK;
 }
 

@@ -596,6 +596,82 @@ def pin_fp8_accumulate_two_roundings(lib):
     assert c[0] == 0x7E and not np.any(c[1:])
 
 
+# ---------------------------------------------------------------------------
+# qgZ hierarchy: tensor-slice reordering and the two-hop reduce ([ZeRO++]
+# sections "Two-hop communication prevents QGZ traffic from multiplying across
+# GPUs" and "Tensor-slice reordering fixes incorrect gradient placement").
+# ---------------------------------------------------------------------------
+_M = 1024  # chunk elements
+
+
+def pin_reordered_quantize_identity(lib):
+    """With one node, or one GPU per node, the reordering is the identity, so
+    the reordered quantization equals the plain one byte for byte."""
+    for A, L in ((1, 4), (4, 1)):
+        x = rng(A * 10 + L).standard_normal(A * L * _M).astype(np.float32)
+        for fmt, G in ((O.INT4, 128), (O.INT6, 32), (O.E4M3, 256)):
+            c, sc = O.quantize_reordered(x, fmt, G, A, L, lib=lib)
+            wc, ws = O.quantize(x, fmt, G, lib=lib)
+            assert np.array_equal(c, wc) and np.array_equal(sc.view(np.uint32), ws.view(np.uint32))
+
+
+def pin_two_hop_ownership(lib):
+    """A gradient that is zero except for chunk c* on GPU g* reaches, after the
+    two hops, GPU c* (the chunk's owner) and no other GPU: the goal the pages
+    give for the reordering."""
+    for A, L in ((2, 2), (2, 4), (4, 2), (3, 2)):
+        P, n = A * L, A * L * _M
+        for g_star, c_star in ((0, P - 1), (P - 1, 0), (1, 2 % P), (P // 2, (P // 2 + 1) % P)):
+            xs = [np.zeros(n, np.float32) for _ in range(P)]
+            xs[g_star][c_star * _M:(c_star + 1) * _M] = rng(g_star).standard_normal(_M)
+            q = [O.quantize_reordered(x, O.INT4, 128, A, L, lib=lib) for x in xs]
+            _, out, sums = O.reduce_two_hop([c for c, _ in q], [sc for _, sc in q], A, L, n, O.INT4,
+                                            128, O.INT8, 64, O.INT4, 128, want_sum=True, lib=lib)
+            for g in range(P):
+                nonzero = np.any(out[g][0] != 0) or np.any(out[g][1] != 0) or np.any(sums[g] != 0)
+                assert nonzero == (g == c_star), (A, L, g_star, c_star, g)
+
+
+def pin_two_hop_exact_sums(lib):
+    """int8 blocks with absmax 127 * 2^k (scale 2^k, exact), one GPU of each
+    node nonzero per block (so the hop-1 sum is that block and requantizing it
+    is exact): the final fp32 sums equal the integer sum over all P GPUs."""
+    k, G = -9, 32
+    for A, L in ((2, 2), (2, 4), (4, 2)):
+        P, n = A * L, A * L * _M
+        nb = n // G
+        ints = []
+        for g in range(P):
+            r = np.random.default_rng([5, g])
+            q = r.integers(-127, 128, n)
+            q[::G] = 127 * np.where(r.random(nb) < 0.5, 1, -1)
+            active = (np.arange(nb) % L) == (g % L)
+            ints.append(np.where(np.repeat(active, G), q, 0).astype(np.int64))
+        xs = [(q * 2.0 ** k).astype(np.float32) for q in ints]
+        qs = [O.quantize_reordered(x, O.INT8, G, A, L, lib=lib) for x in xs]
+        _, out, sums = O.reduce_two_hop([c for c, _ in qs], [sc for _, sc in qs], A, L, n, O.INT8, G,
+                                        O.INT8, G, O.INT8, G, want_sum=True, lib=lib)
+        total = np.sum(ints, axis=0)
+        for g in range(P):
+            want = (total[g * _M:(g + 1) * _M] * 2.0 ** k).astype(np.float32)
+            assert np.array_equal(sums[g], want), (A, L, g)
+
+
+def pin_two_hop_order(lib):
+    """Each hop sums in GPU order: with values 1, 2^-24, 2^-24 (int2 codes, so
+    the scale is the value itself), summing left to right gives 1 and right to
+    left 1 + 2^-23. Three nodes of one GPU test hop 2; one node of three GPUs
+    tests hop 1 (its sum survives the int2 requantization as the scale)."""
+    vals = [1.0, 2.0 ** -24, 2.0 ** -24]
+    for A, L in ((3, 1), (1, 3)):
+        n = 3 * _M
+        q = [O.quantize_reordered(np.full(n, np.float32(v)), O.INT2, 32, A, L, lib=lib) for v in vals]
+        _, out, sums = O.reduce_two_hop([c for c, _ in q], [sc for _, sc in q], A, L, n, O.INT2, 32,
+                                        O.INT2, 32, O.INT8, 32, want_sum=True, lib=lib)
+        for g in range(3):
+            assert np.all(sums[g] == np.float32(1.0)), (A, L, g)
+
+
 FAST_PINS = [
     pin_bpw_endpoints, pin_bpw_formula, pin_zeropp_payload, pin_bit_layout,
     pin_e4m3_points, pin_e4m3_vs_library, pin_f16_vs_library, pin_bf16_vs_library,
@@ -604,4 +680,6 @@ FAST_PINS = [
     pin_idempotence, pin_dequant_values, pin_reduce_single_shard, pin_reduce_pow2_exact,
     pin_reduce_order, pin_reduce_plain_sum_and_bound, pin_reduce_two_roundings,
     pin_fp8_reduce_no_overflow, pin_fp8_accumulate, pin_fp8_accumulate_two_roundings,
+    pin_reordered_quantize_identity, pin_two_hop_ownership, pin_two_hop_exact_sums,
+    pin_two_hop_order,
 ]

@@ -57,6 +57,27 @@ MUTANTS = [
      "int64_t lo = k * G, len = (n - lo < G) ? n - lo - 1 : G;\n"
      "        for (i = 0; i < len; ++i) scratch[i] = load_elem(src, dtype, lo + i);"),
     ("codes_not_cleared", "memset(codes, 0, (size_t)orc_codes_bytes(fmt, n));", ""),
+    ("reorder_identity", "static int64_t slice_position(int64_t c, int A, int L) { return (c % L) * A + c / L; }",
+     "static int64_t slice_position(int64_t c, int A, int L) { (void)A; (void)L; return c; }"),
+    ("hop1_wrong_part", "            int64_t off = (int64_t)l * A * m;",
+     "            int64_t off = (int64_t)((l + 1) % L) * A * m;"),
+    ("hop2_wrong_chunk", "            int64_t off = (int64_t)a * m;",
+     "            int64_t off = (int64_t)((a + 1) % A) * m;"),
+    ("hop1_reverse_order",
+     "                sc[r] = codes[a * L + r] + off * code_bits(fmt_in) / 8;\n"
+     "                ss[r] = scales[a * L + r] + off / G_in;",
+     "                sc[r] = codes[a * L + (L - 1 - r)] + off * code_bits(fmt_in) / 8;\n"
+     "                ss[r] = scales[a * L + (L - 1 - r)] + off / G_in;"),
+    ("hop2_reverse_order",
+     "                sc[r] = mid_codes[r * L + l] + off * code_bits(fmt_mid) / 8;\n"
+     "                ss[r] = mid_scales[r * L + l] + off / G_mid;",
+     "                sc[r] = mid_codes[(A - 1 - r) * L + l] + off * code_bits(fmt_mid) / 8;\n"
+     "                ss[r] = mid_scales[(A - 1 - r) * L + l] + off / G_mid;"),
+    ("hop2_wrong_owner",
+     "            rc = orc_reduce(sc, ss, A, m, fmt_mid, G_mid, out_codes[a * L + l],\n"
+     "                            out_scales[a * L + l], fmt_out, G_out, sums ? sums[a * L + l] : 0);",
+     "            rc = orc_reduce(sc, ss, A, m, fmt_mid, G_mid, out_codes[l * A + a],\n"
+     "                            out_scales[l * A + a], fmt_out, G_out, sums ? sums[l * A + a] : 0);"),
 ]
 
 
