@@ -67,6 +67,11 @@ def _declare(L):
     L.zq_last_cuda_error.restype = i32
     L.zq_device_status.argtypes = [vp]
     L.zq_device_status.restype = i32
+    L.zq_quantize_reordered.argtypes = [vp, i32, i64, i32, i64, i32, i32, vp, vp, vp]
+    L.zq_quantize_reordered.restype = i32
+    L.zq_reduce_two_hop.argtypes = [vp, vp, i32, i32, i64, i32, i64, vp, vp, i32, i64, vp, vp, i32,
+                                    i64, vp, vp]
+    L.zq_reduce_two_hop.restype = i32
     return L
 
 
@@ -181,6 +186,53 @@ def _reduce(entry: str, codes_list, scales_list, n, fmt_in, G_in, fmt_out, G_out
                                  sum_out.data_ptr() if sum_out is not None else None,
                                  _stream(out_codes, stream)), entry)
     return out_codes, out_scales, sum_out
+
+
+def quantize_reordered(src, fmt: int, G: int, nodes: int, gpus_per_node: int, codes=None,
+                       scales=None, stream=None):
+    """Quantize with qgZ's tensor-slice reordering (see zq_quantize_reordered)."""
+    _cuda_contig(src, "src")
+    n = src.numel()
+    codes = empty_codes(fmt, n, src.device) if codes is None else codes
+    scales = empty_scales(n, G, src.device) if scales is None else scales
+    _check(lib().zq_quantize_reordered(src.data_ptr(), dtype_code(src.dtype), n, fmt, G, nodes,
+                                       gpus_per_node, codes.data_ptr(), scales.data_ptr(),
+                                       _stream(src, stream)), "zq_quantize_reordered")
+    return codes, scales
+
+
+def reduce_two_hop(codes_list, scales_list, nodes: int, gpus_per_node: int, n: int, fmt_in: int,
+                   G_in: int, fmt_mid: int, G_mid: int, fmt_out: int, G_out: int, mid=None,
+                   out=None, sums=None, stream=None):
+    """qgZ's two-hop reduce over P = nodes * gpus_per_node simulated GPUs (see
+    zq_reduce_two_hop). mid / out: lists of (codes, scales) per GPU, allocated
+    when None; sums: None, True (allocate) or a list of fp32 tensors.
+    Returns (mid, out, sums)."""
+    torch = _torch()
+    P = nodes * gpus_per_node
+    if len(codes_list) != P or len(scales_list) != P:
+        raise ValueError("need one codes and one scales tensor per GPU")
+    dev = codes_list[0].device
+    m = n // P
+    if mid is None:
+        mid = [(empty_codes(fmt_mid, nodes * m, dev), empty_scales(nodes * m, G_mid, dev))
+               for _ in range(P)]
+    if out is None:
+        out = [(empty_codes(fmt_out, m, dev), empty_scales(m, G_out, dev)) for _ in range(P)]
+    if sums is True:
+        sums = [torch.empty(m, dtype=torch.float32, device=dev) for _ in range(P)]
+
+    def arr(ts):
+        return (ctypes.c_void_p * P)(*[t.data_ptr() for t in ts])
+
+    ic, is_ = arr(codes_list), arr(scales_list)
+    mc, ms = arr([c for c, _ in mid]), arr([s for _, s in mid])
+    oc, os_ = arr([c for c, _ in out]), arr([s for _, s in out])
+    sp = arr(sums) if sums is not None else None
+    _check(lib().zq_reduce_two_hop(ic, is_, nodes, gpus_per_node, n, fmt_in, G_in, mc, ms, fmt_mid,
+                                   G_mid, oc, os_, fmt_out, G_out, sp,
+                                   _stream(codes_list[0], stream)), "zq_reduce_two_hop")
+    return mid, out, sums
 
 
 def reduce_quantized(codes_list, scales_list, n: int, fmt_in: int, G_in: int, fmt_out: int,

@@ -7,6 +7,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "zq.h"
 #include "zq_host.h"
@@ -212,6 +213,126 @@ zq_status zq_quantize(const void *src, int src_dtype, int64_t n, int format, int
   const bool wide = aligned32(src);
   return from_cuda(launch_quantize(src, src_dtype, n, format, G, codes, scales, as_stream(stream),
                                    wide));
+}
+
+zq_status zq_quantize_reordered(const void *src, int src_dtype, int64_t n, int format, int64_t G,
+                                int nodes, int gpus_per_node, void *codes, float *scales,
+                                void *stream) {
+  if (!bits_of(format) || !elem_bytes(src_dtype)) return ZQ_ERR_UNSUPPORTED;
+  if (nodes < 1 || gpus_per_node < 1 || nodes * gpus_per_node > ZQ_MAX_SHARDS)
+    return ZQ_ERR_INVALID_ARG;
+  const int64_t P = int64_t(nodes) * gpus_per_node;
+  if (n < 0 || !valid_block(G) || n % (P * 1024) != 0) return ZQ_ERR_INVALID_ARG;
+  if (n == 0) return ZQ_OK;
+  if (!src || !codes || !scales) return ZQ_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(codes) || !aligned16(scales)) return ZQ_ERR_MISALIGNED;
+  const Range rs(src, size_t(n) * elem_bytes(src_dtype)), rc(codes, zq_codes_bytes(format, n)),
+      rk(scales, size_t(zq_num_blocks(n, G)) * 4u);
+  if (rc.overlaps(rs) || rk.overlaps(rs) || rc.overlaps(rk)) return ZQ_ERR_ALIAS;
+  for (const void *p : {static_cast<const void *>(src), static_cast<const void *>(codes),
+                        static_cast<const void *>(scales)})
+    if (zq_status st = check_device_ptr(p)) return st;
+  const SliceRemap rm{nodes, gpus_per_node, n / (P * 1024)};
+  return from_cuda(launch_quantize(src, src_dtype, n, format, G, codes, scales, as_stream(stream),
+                                   aligned32(src), rm));
+}
+
+zq_status zq_reduce_two_hop(const void *const *codes, const float *const *scales, int nodes,
+                            int gpus_per_node, int64_t n, int format_in, int64_t G_in,
+                            void *const *mid_codes, float *const *mid_scales, int format_mid,
+                            int64_t G_mid, void *const *out_codes, float *const *out_scales,
+                            int format_out, int64_t G_out, float *const *sums, void *stream) {
+  if (!bits_of(format_in) || !bits_of(format_mid) || !bits_of(format_out))
+    return ZQ_ERR_UNSUPPORTED;
+  if (nodes < 1 || gpus_per_node < 1 || nodes * gpus_per_node > ZQ_MAX_SHARDS)
+    return ZQ_ERR_INVALID_ARG;
+  const int A = nodes, L = gpus_per_node, P = A * L;
+  // chunks of a multiple of 4096 elements keep every per-shard code and scale
+  // slice 16-byte aligned (the reduce kernel reads them with bulk copies)
+  if (n < 0 || !valid_block(G_in) || !valid_block(G_mid) || !valid_block(G_out) ||
+      n % (int64_t(P) * 4096) != 0)
+    return ZQ_ERR_INVALID_ARG;
+  if (n == 0) return ZQ_OK;
+  if (!codes || !scales || !mid_codes || !mid_scales || !out_codes || !out_scales)
+    return ZQ_ERR_INVALID_ARG;
+  const int64_t m = n / P;
+  const int bin = bits_of(format_in), bmid = bits_of(format_mid);
+  // every buffer: present, 16-byte aligned, on this device, and no output
+  // (hop-1 result, final codes, scales, sums) overlapping any other buffer
+  std::vector<Range> inputs, outputs;
+  for (int g = 0; g < P; ++g) {
+    if (!codes[g] || !scales[g] || !mid_codes[g] || !mid_scales[g] || !out_codes[g] ||
+        !out_scales[g] || (sums && !sums[g]))
+      return ZQ_ERR_INVALID_ARG;
+    const void *all[7] = {codes[g], scales[g], mid_codes[g], mid_scales[g], out_codes[g],
+                          out_scales[g], sums ? sums[g] : nullptr};
+    for (const void *p : all)
+      if (p && !aligned16(p)) return ZQ_ERR_MISALIGNED;
+    inputs.emplace_back(codes[g], zq_codes_bytes(format_in, n));
+    inputs.emplace_back(scales[g], size_t(zq_num_blocks(n, G_in)) * 4u);
+    outputs.emplace_back(mid_codes[g], zq_codes_bytes(format_mid, int64_t(A) * m));
+    outputs.emplace_back(mid_scales[g], size_t(zq_num_blocks(int64_t(A) * m, G_mid)) * 4u);
+    outputs.emplace_back(out_codes[g], zq_codes_bytes(format_out, m));
+    outputs.emplace_back(out_scales[g], size_t(zq_num_blocks(m, G_out)) * 4u);
+    if (sums) outputs.emplace_back(sums[g], size_t(m) * 4u);
+  }
+  for (size_t i = 0; i < outputs.size(); ++i) {
+    for (const Range &r : inputs)
+      if (outputs[i].overlaps(r)) return ZQ_ERR_ALIAS;
+    for (size_t j = i + 1; j < outputs.size(); ++j)
+      if (outputs[i].overlaps(outputs[j])) return ZQ_ERR_ALIAS;
+  }
+  for (int g = 0; g < P; ++g) {
+    const void *all[7] = {codes[g], scales[g], mid_codes[g], mid_scales[g], out_codes[g],
+                          out_scales[g], sums ? sums[g] : nullptr};
+    for (const void *p : all)
+      if (p)
+        if (zq_status st = check_device_ptr(p)) return st;
+  }
+  const cudaStream_t st = as_stream(stream);
+  ReduceArgs a;
+  // hop 1: GPU (node x, local l) sums part l (A*m elements) of the GPUs of node x
+  for (int x = 0; x < A; ++x)
+    for (int l = 0; l < L; ++l) {
+      std::memset(&a, 0, sizeof(a));
+      const int64_t off = int64_t(l) * A * m;
+      for (int r = 0; r < L; ++r) {
+        a.codes[r] = static_cast<const uint8_t *>(codes[x * L + r]) + off * bin / 8;
+        a.scales[r] = scales[x * L + r] + off / G_in;
+        if (!aligned16(a.codes[r]) || !aligned16(a.scales[r])) return ZQ_ERR_MISALIGNED;
+      }
+      a.out_codes = static_cast<uint8_t *>(mid_codes[x * L + l]);
+      a.out_scales = mid_scales[x * L + l];
+      a.n = int64_t(A) * m;
+      a.nshards = L;
+      a.log2Gin = log2_block(G_in);
+      a.log2Gout = log2_block(G_mid);
+      a.wide = 1;
+      a.one = 1.0f;
+      if (zq_status s2 = from_cuda(launch_reduce(a, format_in, format_mid, st))) return s2;
+    }
+  // hop 2: GPU (node x, local l) sums chunk x of the hop-1 results of GPUs (*, l)
+  for (int x = 0; x < A; ++x)
+    for (int l = 0; l < L; ++l) {
+      std::memset(&a, 0, sizeof(a));
+      const int64_t off = int64_t(x) * m;
+      for (int r = 0; r < A; ++r) {
+        a.codes[r] = static_cast<const uint8_t *>(mid_codes[r * L + l]) + off * bmid / 8;
+        a.scales[r] = mid_scales[r * L + l] + off / G_mid;
+        if (!aligned16(a.codes[r]) || !aligned16(a.scales[r])) return ZQ_ERR_MISALIGNED;
+      }
+      a.out_codes = static_cast<uint8_t *>(out_codes[x * L + l]);
+      a.out_scales = out_scales[x * L + l];
+      a.sum_out = sums ? sums[x * L + l] : nullptr;
+      a.n = m;
+      a.nshards = A;
+      a.log2Gin = log2_block(G_mid);
+      a.log2Gout = log2_block(G_out);
+      a.wide = (!a.sum_out || aligned32(a.sum_out)) ? 1 : 0;
+      a.one = 1.0f;
+      if (zq_status s2 = from_cuda(launch_reduce(a, format_mid, format_out, st))) return s2;
+    }
+  return ZQ_OK;
 }
 
 zq_status zq_dequantize(const void *codes, const float *scales, int64_t n, int format, int64_t G,

@@ -72,7 +72,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, size_t smem, cud
 
 // Launchers (one translation unit each). They return the launch status.
 cudaError_t launch_quantize(const void *src, int dt, int64_t n, int fmt, int64_t G, void *codes,
-                            float *scales, cudaStream_t st, bool wide);
+                            float *scales, cudaStream_t st, bool wide,
+                            const SliceRemap &rm = SliceRemap{1, 1, 0});
 cudaError_t launch_dequantize(const void *codes, const float *scales, int64_t n, int fmt,
                               int64_t G, void *dst, int dt, cudaStream_t st, bool wide);
 cudaError_t launch_reduce(const ReduceArgs &a, int fin, int fout, cudaStream_t st);

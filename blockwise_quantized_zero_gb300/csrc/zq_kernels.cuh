@@ -49,6 +49,24 @@ struct WarpCursor {
 // ===========================================================================
 // Quantize
 // ===========================================================================
+// Tensor-slice reordering of the output tiles (qgZ): the tensor is P = A*L
+// chunks of tpc tiles, and chunk c = a*L + l is written at slice position
+// l*A + a (the transpose of the A x L chunk grid). tpc == 0: no reordering.
+struct SliceRemap {
+  int A, L;
+  int64_t tpc;
+  __device__ __forceinline__ int64_t out_tile(int64_t t) const {
+    if (tpc == 0) return t;
+    const uint32_t c = uint32_t(t / tpc), cl = c % uint32_t(L);
+    return (int64_t(cl) * A + c / uint32_t(L)) * tpc + (t - int64_t(c) * tpc);
+  }
+  __device__ __forceinline__ int64_t in_tile(int64_t o) const {
+    if (tpc == 0) return o;
+    const uint32_t p = uint32_t(o / tpc), pa = p % uint32_t(A);
+    return (int64_t(pa) * L + p / uint32_t(A)) * tpc + (o - int64_t(p) * tpc);
+  }
+};
+
 // Block scales of one tile. Lane l computes the scale (IEEE division) and
 // its reciprocal for block l of the tile (there are 1024 / G <= 32 blocks),
 // stores it, and the values are shuffled back to the lanes of each block.
@@ -104,7 +122,8 @@ template <int DT> struct FixQueue {
 template <int DT, int FMT, int G>
 __device__ __noinline__ void quantize_flush(FixQueue<DT> &fq, int w, int first, int count,
                                             const void *__restrict__ src,
-                                            uint8_t *__restrict__ codes, int lane, bool wide) {
+                                            uint8_t *__restrict__ codes, int lane, bool wide,
+                                            const SliceRemap rm) {
   constexpr int B = Fmt<FMT>::kBits, W = Fmt<FMT>::kWords16;
   __syncwarp();  // queue entries and fast-path codes of all lanes are visible
   for (int base = 0; base < count; base += 32) {
@@ -117,8 +136,8 @@ __device__ __noinline__ void quantize_flush(FixQueue<DT> &fq, int w, int first, 
       if constexpr (kStash<DT>) {
 #pragma unroll
         for (int k = 0; k < kRawWords<DT>; ++k) raw[k] = fq.raw[w][slot][k];
-      } else {
-        load16_raw<DT>(src, e, raw, wide);
+      } else {  // e is the output position; the source is read at the input one
+        load16_raw<DT>(src, rm.in_tile(e / kTile) * kTile + e % kTile, raw, wide);
       }
       float x[kVec];
       widen16<DT>(raw, x);
@@ -219,7 +238,8 @@ template <int DT, int FMT, int G>
 __global__ void __launch_bounds__(kThreads, 3) quantize_kernel(const void *__restrict__ src,
                                                             uint8_t *__restrict__ codes,
                                                             float *__restrict__ scales,
-                                                            int64_t n, int wide) {
+                                                            int64_t n, int wide,
+                                                            const SliceRemap rm) {
   const WarpCursor c;
   const int64_t nfull = n / kTile;
   const bool wd = wide != 0;
@@ -246,13 +266,13 @@ __global__ void __launch_bounds__(kThreads, 3) quantize_kernel(const void *__res
       for (int j = 0; j < kU; ++j)
         load16_raw<DT>(src, tn * kTile + j * kRun + c.lane * kVec, raw[j], wd);
     }
-    quantize_tile<DT, FMT, G>(cur, codes, scales, t * kTile, c.lane, fq, w, count);
+    quantize_tile<DT, FMT, G>(cur, codes, scales, rm.out_tile(t) * kTile, c.lane, fq, w, count);
     while (count >= 32) {  // fix full batches right away, newest first
       count -= 32;
-      quantize_flush<DT, FMT, G>(fq, w, count, 32, src, codes, c.lane, wd);
+      quantize_flush<DT, FMT, G>(fq, w, count, 32, src, codes, c.lane, wd, rm);
     }
   }
-  if (count) quantize_flush<DT, FMT, G>(fq, w, 0, count, src, codes, c.lane, wd);
+  if (count) quantize_flush<DT, FMT, G>(fq, w, 0, count, src, codes, c.lane, wd, rm);
   if (c.owns_tail(n)) quantize_tail<DT, FMT, G>(src, codes, scales, nfull * kTile, n, c.lane);
 }
 

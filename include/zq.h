@@ -171,6 +171,58 @@ zq_status zq_reduce_quantized_static(const void *const *codes, const float *cons
                                      int64_t G_out, float *sum_out, void *stream);
 
 /*
+ * zq_quantize_reordered -- zq_quantize fused with qgZ's tensor-slice
+ * reordering ([ZeRO++] sections "Tensor-slice reordering fixes incorrect
+ * gradient placement" and "The implementation combines kernel fusion with
+ * communication overlap": the reordering is fused into the quantization).
+ * The n elements are P = nodes * gpus_per_node chunks of n / P elements;
+ * chunk c (the chunk GPU c owns after the reduce-scatter, c = a *
+ * gpus_per_node + l for GPU l of node a) is quantized on its own and its codes
+ * and scales are stored at slice position l * nodes + a (the transpose of the
+ * nodes x gpus_per_node grid of chunks), so that part l of the output holds,
+ * node by node, the chunks that GPU l of every node will own.
+ *   nodes, gpus_per_node  >= 1, product <= ZQ_MAX_SHARDS
+ *   n                     a multiple of 1024 * nodes * gpus_per_node
+ * Other arguments, layout and errors as zq_quantize. With one node or one
+ * GPU per node the result equals zq_quantize's.
+ */
+zq_status zq_quantize_reordered(const void *src, int src_dtype, int64_t n, int format, int64_t G,
+                                int nodes, int gpus_per_node, void *codes, float *scales,
+                                void *stream);
+
+/*
+ * zq_reduce_two_hop -- qgZ's two-hop quantized reduce ([ZeRO++] sections "Two-
+ * hop communication prevents QGZ traffic from multiplying across GPUs" and
+ * "The implementation combines kernel fusion with communication overlap"),
+ * with the P = nodes * gpus_per_node GPUs simulated as buffers on this GPU.
+ * GPU g = a * gpus_per_node + l holds codes[g], scales[g]: n elements in the
+ * layout of zq_quantize_reordered (format_in, G_in). With m = n / P:
+ *   hop 1 (intra-node; the dequantize + reduce fused with the requantization
+ *     for the inter-node step): mid[g] = requantize(format_mid, G_mid) of the
+ *     shard-ordered fp32 sum over l2 = 0..gpus_per_node-1 of part l (the
+ *     nodes * m elements at offset l * nodes * m) of GPU a * gpus_per_node + l2;
+ *   hop 2 (inter-node): out[g] = requantize(format_out, G_out) of the
+ *     node-ordered fp32 sum over a2 = 0..nodes-1 of chunk a (the m elements at
+ *     offset a * m) of mid[a2 * gpus_per_node + l]; sums[g] (optional) receives
+ *     those fp32 sums. out[g] is the reduced chunk g.
+ * Each sum is exactly zq_reduce_quantized's (+0.0f, then one binary32 add per
+ * term in the order given); the hop-1 results pass through format_mid, as the
+ * pages' protocol sends them. 2 * P reduce launches are enqueued on `stream`.
+ *   all pointer arrays   HOST arrays of P device pointers; mid_codes[g] holds
+ *                        zq_codes_bytes(format_mid, nodes * m) bytes and
+ *                        mid_scales[g] zq_num_blocks(nodes * m, G_mid) floats;
+ *                        out_codes[g] / out_scales[g] / sums[g]: m elements
+ *   sums                 NULL, or an array of P device pointers
+ *   n                    a multiple of 4096 * P (keeps every slice 16-byte aligned)
+ * Errors as zq_reduce_quantized; no output may overlap any input or output.
+ */
+zq_status zq_reduce_two_hop(const void *const *codes, const float *const *scales, int nodes,
+                            int gpus_per_node, int64_t n, int format_in, int64_t G_in,
+                            void *const *mid_codes, float *const *mid_scales, int format_mid,
+                            int64_t G_mid, void *const *out_codes, float *const *out_scales,
+                            int format_out, int64_t G_out, float *const *sums, void *stream);
+
+/*
  * zq_fp8_accumulate -- in-place FP8 gradient accumulation ([AGoQ] 2.B "Local
  * Accumulation", with the addition in fp32):
  *   v_i = fl32(fl32(e4m3(c_i) * s_block) + g_i), then the block is requantized
