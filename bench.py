@@ -520,6 +520,125 @@ class QgzReduce:
                              "single thread")
 
 
+class QgzTwoHop:
+    """qgZ's hierarchy simulated on one GPU: 2 nodes x 4 GPUs, each holding a
+    134,217,728-element fp32 gradient ~ Laplace(0, 1e-4) (seed 3, stream = GPU,
+    like qgz_reduce's shards). A step quantizes every gradient to int4 G=128
+    with tensor-slice reordering, then runs the two-hop reduce: intra-node
+    reduce + requantize to int4 G=128, inter-node reduce + requantize to int4
+    G=128 (2 x 8 reduce launches)."""
+
+    name = "qgz_two_hop"
+    dtype = "fp32 gradients in, int4 codes + fp32 scales between the hops and out"
+    A, L = 2, 4
+    n = 134217728
+
+    def config(self):
+        return {"workload": "qgz_two_hop: 2 nodes x 4 GPUs simulated as buffers, 134,217,728 fp32 "
+                            "gradients ~Laplace(0,1e-4) per GPU; quantize with tensor-slice "
+                            "reordering (int4 G=128), intra-node reduce -> int4 G=128, inter-node "
+                            "reduce -> int4 G=128",
+                "elements_per_gpu": self.n, "nodes": self.A, "gpus_per_node": self.L,
+                "l2": "no flush: 512 MB of fp32 gradient per quantize launch, 35-71 MB of codes "
+                      "per reduce launch, 0.9 GB of codes per step >> 126 MB L2"}
+
+    def setup(self):
+        import torch
+
+        import blockwise_quantized_zero_gb300 as zq
+        from blockwise_quantized_zero_gb300 import inputs
+
+        self.zq = zq
+        P, n = self.A * self.L, self.n
+        self.P, self.m = P, n // P
+        self.x, self.host_sample = [], []
+        for g in range(P):
+            h = inputs.gradient_shard_f32(n, shard=g)
+            self.host_sample.append(h[: 1 << 24].copy())
+            self.x.append(torch.from_numpy(h).cuda())
+            del h
+        self.q = [(zq.empty_codes(zq.INT4, n, "cuda"), zq.empty_scales(n, 128, "cuda"))
+                  for _ in range(P)]
+        am = self.A * self.m
+        self.mid = [(zq.empty_codes(zq.INT4, am, "cuda"), zq.empty_scales(am, 128, "cuda"))
+                    for _ in range(P)]
+        self.out = [(zq.empty_codes(zq.INT4, self.m, "cuda"), zq.empty_scales(self.m, 128, "cuda"))
+                    for _ in range(P)]
+
+    def _reduce_bytes(self, k=1):
+        P, A, L, m = self.P, self.A, self.L, self.m
+        hop1 = P * (L + 1) * packed_bytes(4, A * m, 128)
+        hop2 = P * (A + 1) * packed_bytes(4, m, 128)
+        return hop1 + hop2
+
+    def two_hop(self):
+        zq = self.zq
+        zq.reduce_two_hop([c for c, _ in self.q], [s for _, s in self.q], self.A, self.L, self.n,
+                          zq.INT4, 128, zq.INT4, 128, zq.INT4, 128, mid=self.mid, out=self.out)
+
+    def launches(self):
+        zq, n = self.zq, self.n
+        out = []
+        for g in range(self.P):
+            out.append(Launch(f"quantize reordered fp32 int4 G=128 GPU {g}", "quantize",
+                              4 * n + packed_bytes(4, n, 128),
+                              lambda g=g: zq.quantize_reordered(self.x[g], zq.INT4, 128, self.A,
+                                                                self.L, *self.q[g])))
+        out.append(Launch("two-hop reduce (2 x 8 launches, int4 G=128)", "reduce",
+                          self._reduce_bytes(), self.two_hop, kernels=2 * self.P))
+        return out
+
+    def setup_e2e(self):
+        import torch
+
+        self.h_x = [x.cpu().pin_memory() for x in self.x]
+        self.h_out = [(torch.empty(c.numel(), dtype=torch.uint8).pin_memory(),
+                       torch.empty(s.numel(), dtype=torch.float32).pin_memory())
+                      for c, s in self.out]
+        d2h = sum(c.numel() + 4 * s.numel() for c, s in self.out)
+        return sum(4 * x.numel() for x in self.x), d2h
+
+    def e2e_bytes(self):
+        return self.step_bytes()
+
+    def step_bytes(self):
+        return self.P * (4 * self.n + packed_bytes(4, self.n, 128)) + self._reduce_bytes()
+
+    def e2e_step(self):
+        """Every GPU's fp32 gradient from host memory, the reduced chunks to host memory."""
+        zq = self.zq
+        for g in range(self.P):
+            self.x[g].copy_(self.h_x[g], non_blocking=True)
+            zq.quantize_reordered(self.x[g], zq.INT4, 128, self.A, self.L, *self.q[g])
+        self.two_hop()
+        for (c, s), (hc, hs) in zip(self.out, self.h_out):
+            hc.copy_(c, non_blocking=True)
+            hs.copy_(s, non_blocking=True)
+
+    def oracle_sample(self, sample=1 << 24):
+        import oracle as O
+        from blockwise_quantized_zero_gb300 import inputs
+
+        P = self.A * self.L
+        sample = max(P * 4096, sample - sample % (P * 4096))
+        host = getattr(self, "host_sample", None)
+        if host is None or host[0].size < sample:
+            host = [inputs.gradient_shard_f32(sample, shard=g) for g in range(P)]
+        xs = [np.ascontiguousarray(x[:sample]) for x in host]
+
+        def run():
+            qs = [O.quantize_reordered(x, O.INT4, 128, self.A, self.L) for x in xs]
+            O.reduce_two_hop([c for c, _ in qs], [s for _, s in qs], self.A, self.L, sample,
+                             O.INT4, 128, O.INT4, 128, O.INT4, 128)
+
+        m = sample // P
+        nbytes = (P * (4 * sample + packed_bytes(4, sample, 128))
+                  + P * (self.L + 1) * packed_bytes(4, self.A * m, 128)
+                  + P * (self.A + 1) * packed_bytes(4, m, 128))
+        return run, nbytes, (f"first {sample:,} elements of each of the 8 GPUs' gradients, "
+                             "reordered quantize and both hops, single thread")
+
+
 class AgoqFP8:
     """E4M3 main gradient of 268,435,456 elements, G=128; a step adds 4
     micro-batch bf16 gradients ~ N(0, 1e-3) (seed 4, stream = micro-batch) in
@@ -753,7 +872,7 @@ class Llama70B:
 
 
 WORKLOADS = {"gm_sweep": GMSweep, "qwz_fp16": QwzFP16, "qgz_reduce": QgzReduce,
-             "agoq_fp8": AgoqFP8, "llama70b": Llama70B}
+             "agoq_fp8": AgoqFP8, "llama70b": Llama70B, "qgz_two_hop": QgzTwoHop}
 
 
 # ---------------------------------------------------------------------------
