@@ -290,48 +290,62 @@ zq_status zq_reduce_two_hop(const void *const *codes, const float *const *scales
         if (zq_status st = check_device_ptr(p)) return st;
   }
   const cudaStream_t st = as_stream(stream);
-  ReduceArgs a;
+  // every shard slice the hops read starts 16-byte aligned (n is a multiple of
+  // 4096 * P); checked again here because the kernels read them with bulk copies
+  for (int g = 0; g < P; ++g)
+    for (int64_t off : {int64_t(0), m, int64_t(A) * m}) {
+      if (!aligned16(static_cast<const uint8_t *>(codes[g]) + off * bin / 8) ||
+          !aligned16(scales[g] + off / G_in) ||
+          !aligned16(static_cast<const uint8_t *>(mid_codes[g]) + off * bmid / 8) ||
+          !aligned16(mid_scales[g] + off / G_mid))
+        return ZQ_ERR_MISALIGNED;
+    }
+  HopArgs h;
   // hop 1: GPU (node x, local l) sums part l (A*m elements) of the GPUs of node x
-  for (int x = 0; x < A; ++x)
-    for (int l = 0; l < L; ++l) {
-      std::memset(&a, 0, sizeof(a));
-      const int64_t off = int64_t(l) * A * m;
-      for (int r = 0; r < L; ++r) {
-        a.codes[r] = static_cast<const uint8_t *>(codes[x * L + r]) + off * bin / 8;
-        a.scales[r] = scales[x * L + r] + off / G_in;
-        if (!aligned16(a.codes[r]) || !aligned16(a.scales[r])) return ZQ_ERR_MISALIGNED;
-      }
-      a.out_codes = static_cast<uint8_t *>(mid_codes[x * L + l]);
-      a.out_scales = mid_scales[x * L + l];
-      a.n = int64_t(A) * m;
-      a.nshards = L;
-      a.log2Gin = log2_block(G_in);
-      a.log2Gout = log2_block(G_mid);
-      a.wide = 1;
-      a.one = 1.0f;
-      if (zq_status s2 = from_cuda(launch_reduce(a, format_in, format_mid, st))) return s2;
-    }
+  std::memset(&h, 0, sizeof(h));
+  for (int g = 0; g < P; ++g) {
+    h.in_codes[g] = static_cast<const uint8_t *>(codes[g]);
+    h.in_scales[g] = scales[g];
+    h.out_codes[g] = static_cast<uint8_t *>(mid_codes[g]);
+    h.out_scales[g] = mid_scales[g];
+  }
+  h.n = int64_t(A) * m;
+  h.part = int64_t(A) * m;
+  h.nprob = P;
+  h.nshards = L;
+  h.log2Gin = log2_block(G_in);
+  h.log2Gout = log2_block(G_mid);
+  h.wide = 1;
+  h.one = 1.0f;
+  h.hop = 1;
+  h.A = A;
+  h.L = L;
+  h.bits_in = bin;
+  if (zq_status s2 = from_cuda(launch_reduce_hop(h, format_in, format_mid, st))) return s2;
   // hop 2: GPU (node x, local l) sums chunk x of the hop-1 results of GPUs (*, l)
-  for (int x = 0; x < A; ++x)
-    for (int l = 0; l < L; ++l) {
-      std::memset(&a, 0, sizeof(a));
-      const int64_t off = int64_t(x) * m;
-      for (int r = 0; r < A; ++r) {
-        a.codes[r] = static_cast<const uint8_t *>(mid_codes[r * L + l]) + off * bmid / 8;
-        a.scales[r] = mid_scales[r * L + l] + off / G_mid;
-        if (!aligned16(a.codes[r]) || !aligned16(a.scales[r])) return ZQ_ERR_MISALIGNED;
-      }
-      a.out_codes = static_cast<uint8_t *>(out_codes[x * L + l]);
-      a.out_scales = out_scales[x * L + l];
-      a.sum_out = sums ? sums[x * L + l] : nullptr;
-      a.n = m;
-      a.nshards = A;
-      a.log2Gin = log2_block(G_mid);
-      a.log2Gout = log2_block(G_out);
-      a.wide = (!a.sum_out || aligned32(a.sum_out)) ? 1 : 0;
-      a.one = 1.0f;
-      if (zq_status s2 = from_cuda(launch_reduce(a, format_mid, format_out, st))) return s2;
-    }
+  std::memset(&h, 0, sizeof(h));
+  bool wide = true;
+  for (int g = 0; g < P; ++g) {
+    h.in_codes[g] = static_cast<const uint8_t *>(mid_codes[g]);
+    h.in_scales[g] = mid_scales[g];
+    h.out_codes[g] = static_cast<uint8_t *>(out_codes[g]);
+    h.out_scales[g] = out_scales[g];
+    h.sums[g] = sums ? sums[g] : nullptr;
+    if (sums && !aligned32(sums[g])) wide = false;
+  }
+  h.n = m;
+  h.part = m;
+  h.nprob = P;
+  h.nshards = A;
+  h.log2Gin = log2_block(G_mid);
+  h.log2Gout = log2_block(G_out);
+  h.wide = wide ? 1 : 0;
+  h.one = 1.0f;
+  h.hop = 2;
+  h.A = A;
+  h.L = L;
+  h.bits_in = bmid;
+  if (zq_status s2 = from_cuda(launch_reduce_hop(h, format_mid, format_out, st))) return s2;
   return ZQ_OK;
 }
 

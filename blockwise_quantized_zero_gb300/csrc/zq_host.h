@@ -77,6 +77,8 @@ cudaError_t launch_quantize(const void *src, int dt, int64_t n, int fmt, int64_t
 cudaError_t launch_dequantize(const void *codes, const float *scales, int64_t n, int fmt,
                               int64_t G, void *dst, int dt, cudaStream_t st, bool wide);
 cudaError_t launch_reduce(const ReduceArgs &a, int fin, int fout, cudaStream_t st);
+// All P reduces of one hop of the two-hop reduce in one launch.
+cudaError_t launch_reduce_hop(const HopArgs &a, int fin, int fout, cudaStream_t st);
 // The same reduce with up to kStaticMaxShards shards whose pointers (host
 // arrays) are copied into a static device table on the stream.
 cudaError_t launch_reduce_static(const void *const *codes, const float *const *scales,

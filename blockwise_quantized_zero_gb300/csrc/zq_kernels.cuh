@@ -357,8 +357,13 @@ struct ReduceArgs {
   int log2Gout;
   int wide;
   float one;  // 1.0f, passed at run time (see accumulate16)
-  __device__ const uint8_t *shard_codes(int r) const { return codes[r]; }
-  __device__ const float *shard_scales(int r) const { return scales[r]; }
+  // one problem per launch
+  __device__ int problems() const { return 1; }
+  __device__ const uint8_t *shard_codes(int, int r) const { return codes[r]; }
+  __device__ const float *shard_scales(int, int r) const { return scales[r]; }
+  __device__ uint8_t *out_codes_of(int) const { return out_codes; }
+  __device__ float *out_scales_of(int) const { return out_scales; }
+  __device__ float *sum_out_of(int) const { return sum_out; }
 };
 
 // The same arguments with the shard pointers in a device-memory table instead
@@ -379,9 +384,67 @@ struct TableReduceArgs {
   int log2Gout;
   int wide;
   float one;
-  __device__ const uint8_t *shard_codes(int r) const { return tab->codes[r]; }
-  __device__ const float *shard_scales(int r) const { return tab->scales[r]; }
+  __device__ int problems() const { return 1; }
+  __device__ const uint8_t *shard_codes(int, int r) const { return tab->codes[r]; }
+  __device__ const float *shard_scales(int, int r) const { return tab->scales[r]; }
+  __device__ uint8_t *out_codes_of(int) const { return out_codes; }
+  __device__ float *out_scales_of(int) const { return out_scales; }
+  __device__ float *sum_out_of(int) const { return sum_out; }
 };
+
+// One hop of qgZ's two-hop reduce: P problems of equal length in one launch
+// (P = A*L <= kMaxShards GPUs). Problem p = a*L + l is GPU p's reduce. Hop 1:
+// shard r is part l (offset l*part elements, part = A*m) of GPU a*L + r's
+// input. Hop 2: shard r is chunk a (offset a*part, part = m) of GPU r*L + l's
+// hop-1 result.
+struct HopArgs {
+  const uint8_t *in_codes[kMaxShards];  // per GPU
+  const float *in_scales[kMaxShards];
+  uint8_t *out_codes[kMaxShards];       // per problem
+  float *out_scales[kMaxShards];
+  float *sums[kMaxShards];              // entries may be null
+  int64_t n;                            // elements per problem
+  int64_t part;
+  int nprob, nshards, log2Gin, log2Gout, wide;
+  float one;
+  int hop, A, L, bits_in;
+  __device__ int problems() const { return nprob; }
+  __device__ int gpu_of(int p, int r) const { return hop == 1 ? (p / L) * L + r : r * L + p % L; }
+  __device__ int64_t off_of(int p) const {
+    return (hop == 1 ? int64_t(p % L) : int64_t(p / L)) * part;
+  }
+  __device__ const uint8_t *shard_codes(int p, int r) const {
+    return in_codes[gpu_of(p, r)] + off_of(p) * bits_in / 8;
+  }
+  __device__ const float *shard_scales(int p, int r) const {
+    return in_scales[gpu_of(p, r)] + (off_of(p) >> log2Gin);
+  }
+  __device__ uint8_t *out_codes_of(int p) const { return out_codes[p]; }
+  __device__ float *out_scales_of(int p) const { return out_scales[p]; }
+  __device__ float *sum_out_of(int p) const { return sums[p]; }
+};
+
+// One problem of a reduce launch, with the member names the requantization
+// and tail routines use.
+// (The accessors read the kernel parameters where they are used, so that a
+// one-problem launch keeps no copies of its pointers in registers.)
+template <typename A> struct RedView {
+  const A *a;
+  int p;
+  __device__ const uint8_t *shard_codes(int r) const { return a->shard_codes(p, r); }
+  __device__ const float *shard_scales(int r) const { return a->shard_scales(p, r); }
+  __device__ uint8_t *codes_out() const { return a->out_codes_of(p); }
+  __device__ float *scales_out() const { return a->out_scales_of(p); }
+  __device__ float *sums_out() const { return a->sum_out_of(p); }
+  __device__ int64_t n() const { return a->n; }
+  __device__ int nshards() const { return a->nshards; }
+  __device__ int log2Gin() const { return a->log2Gin; }
+  __device__ int log2Gout() const { return a->log2Gout; }
+};
+
+template <typename A> __device__ __forceinline__ RedView<A> view_of(const A &a, int p) {
+  return RedView<A>{&a, p};
+}
 
 // Add shard r's 16 dequantized values into acc: acc = fl(acc + fl(q * s)).
 // ptxas contracts a packed mul.rn.f32x2 feeding a packed add.rn.f32x2 into a
@@ -416,7 +479,7 @@ template <int FOUT, int KU, typename A>
 __device__ __forceinline__ void requant_tile(const A &a, float (&acc)[KU][kVec],
                                              int64_t e0, int lane) {
   constexpr int B = Fmt<FOUT>::kBits, W = Fmt<FOUT>::kWords16;
-  const int lg = a.log2Gout;                 // 5 .. 10, and G <= KU * 512
+  const int lg = a.log2Gout();                 // 5 .. 10, and G <= KU * 512
   float m[KU], s[KU], r[KU];
 #pragma unroll
   for (int j = 0; j < KU; ++j) m[j] = absmax16(acc[j]);
@@ -432,7 +495,7 @@ __device__ __forceinline__ void requant_tile(const A &a, float (&acc)[KU][kVec],
       mb = (lane < per_run) ? mb : m1;
     }
     const float sb = block_scale<FOUT>(mb), rb = safe_rcp(sb);
-    if (lane < per_run * KU) a.out_scales[(e0 >> lg) + lane] = sb;
+    if (lane < per_run * KU) a.scales_out()[(e0 >> lg) + lane] = sb;
 #pragma unroll
     for (int j = 0; j < KU; ++j) {
       const int owner = j * per_run + (lane >> (lg - 4));
@@ -447,7 +510,7 @@ __device__ __forceinline__ void requant_tile(const A &a, float (&acc)[KU][kVec],
       s[j] = sb;
       r[j] = rb;
     }
-    if (lane == 0) a.out_scales[e0 >> lg] = sb;
+    if (lane == 0) a.scales_out()[e0 >> lg] = sb;
   }
   uint32_t w[KU][W];
 #pragma unroll
@@ -457,32 +520,32 @@ __device__ __forceinline__ void requant_tile(const A &a, float (&acc)[KU][kVec],
   }
 #pragma unroll
   for (int j = 0; j < KU; ++j)
-    store_codes16<B>(a.out_codes + (e0 + j * kRun + lane * kVec) * B / 8, w[j]);
+    store_codes16<B>(a.codes_out() + (e0 + j * kRun + lane * kVec) * B / 8, w[j]);
 }
 
 // Sum over shards of element i (tails).
 template <int FIN, typename A> __device__ __forceinline__ float reduce1(const A &a, int64_t i) {
   float acc = 0.0f;
-  for (int r = 0; r < a.nshards; ++r)
-    acc = __fadd_rn(acc, dequant1<FIN>(a.shard_codes(r), i, a.shard_scales(r)[i >> a.log2Gin]));
+  for (int r = 0; r < a.nshards(); ++r)
+    acc = __fadd_rn(acc, dequant1<FIN>(a.shard_codes(r), i, a.shard_scales(r)[i >> a.log2Gin()]));
   return acc;
 }
 
 template <int FIN, int FOUT, typename A>
 __device__ __noinline__ void reduce_tail(const A &a, int64_t e0, int lane) {
   constexpr int B = Fmt<FOUT>::kBits;
-  const int64_t n = a.n, Gout = int64_t(1) << a.log2Gout;
-  uint32_t *cw = reinterpret_cast<uint32_t *>(a.out_codes);
+  const int64_t n = a.n(), Gout = int64_t(1) << a.log2Gout();
+  uint32_t *cw = reinterpret_cast<uint32_t *>(a.codes_out());
   for (int64_t lo = e0; lo < n; lo += Gout) {
     const int64_t hi = (lo + Gout < n) ? lo + Gout : n;
     float m = 0.0f;
     for (int64_t i = lo + lane; i < hi; i += 32) {
       const float v = reduce1<FIN, A>(a, i);
-      if (a.sum_out) a.sum_out[i] = v;
+      if (a.sums_out()) a.sums_out()[i] = v;
       m = fmaxf(m, fabsf(v));
     }
     const float s = block_scale<FOUT>(warp_max(m));
-    if (lane == 0) a.out_scales[lo >> a.log2Gout] = s;
+    if (lane == 0) a.scales_out()[lo >> a.log2Gout()] = s;
     const int64_t len = hi - lo, nwords = (len * B + 31) / 32, w0 = lo * B / 32;
     for (int64_t wi = lane; wi < nwords; wi += 32) {
       const int64_t bit0 = wi * 32, first = bit0 / B;
@@ -565,10 +628,11 @@ __global__ void __launch_bounds__(kRedThreads, 2)
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const uint32_t full0 = smem_addr(red_smem + RG::kBarOff), empty0 = full0 + 8 * S;
   const int64_t nfull = a.n / kTile;                                 // whole 1024-element tiles
-  const int64_t nct = (nfull + kRedConsumers - 1) / kRedConsumers;   // CTA tiles
+  const int64_t nct = (nfull + kRedConsumers - 1) / kRedConsumers;   // CTA tiles per problem
+  const int64_t nctall = nct * a.problems();                         // CTA tiles of the launch
   const int nb = (a.nshards + RG::kShards - 1) / RG::kShards;        // units per CTA tile
   const int64_t mytiles =
-      blockIdx.x < nct ? (nct - 1 - int64_t(blockIdx.x)) / gridDim.x + 1 : 0;
+      blockIdx.x < nctall ? (nctall - 1 - int64_t(blockIdx.x)) / gridDim.x + 1 : 0;
   const int64_t nunits = mytiles * nb;
   const int lgin = a.log2Gin;
   const int nbt = kTile >> lgin;  // input blocks per tile
@@ -585,7 +649,9 @@ __global__ void __launch_bounds__(kRedThreads, 2)
 
   if (w == kRedConsumers) {  // producer warp: lane 0 issues every copy
     if (lane != 0) return;
-    int64_t ct = blockIdx.x;  // cursor (ct, k) of unit u
+    // cursor of unit u: problem p, its CTA tile ct, shard batch k
+    int p = nct > 0 ? int(blockIdx.x / nct) : 0;
+    int64_t ct = blockIdx.x - int64_t(p) * nct;
     int k = 0;
     for (int64_t u = 0; u < nunits; ++u) {
       const int st = int(u % S);
@@ -607,15 +673,15 @@ __global__ void __launch_bounds__(kRedThreads, 2)
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(full, uint32_t(ns) * (cbytes + (stma ? sbytes : 0u)));
       for (int q = 0; q < ns; ++q) {
-        bulk_g2s(dst + q * kRedConsumers * CB, a.shard_codes(r0 + q) + ct * kRedConsumers * CB, cbytes,
-                 full);
+        bulk_g2s(dst + q * kRedConsumers * CB, a.shard_codes(p, r0 + q) + ct * kRedConsumers * CB,
+                 cbytes, full);
         if (stma)
           bulk_g2s(dst + RG::kScaleOff + q * kRedConsumers * nbt * 4,
-                   a.shard_scales(r0 + q) + ct * kRedConsumers * nbt, sbytes, full);
+                   a.shard_scales(p, r0 + q) + ct * kRedConsumers * nbt, sbytes, full);
       }
       if (++k == nb) {
         k = 0;
-        ct += gridDim.x;
+        for (ct += gridDim.x; ct >= nct && p < a.problems(); ct -= nct) ++p;
       }
     }
     return;
@@ -623,8 +689,11 @@ __global__ void __launch_bounds__(kRedThreads, 2)
 
   // consumer warp w: tile w of every CTA tile
   float acc[kU][kVec];
-  int64_t ct = blockIdx.x;  // cursor (ct, k) of unit u
+  // cursor of unit u: problem p, its CTA tile ct, shard batch k
+  int p = nct > 0 ? int(blockIdx.x / nct) : 0;
+  int64_t ct = blockIdx.x - int64_t(p) * nct;
   int k = 0;
+  RedView<A> v = view_of(a, p < a.problems() ? p : 0);
   for (int64_t u = 0; u < nunits; ++u) {
     const int st = int(u % S);
     if (!mbar_wait_warp(full0 + 8 * st, uint32_t(u / S) & 1u)) {
@@ -653,7 +722,7 @@ __global__ void __launch_bounds__(kRedThreads, 2)
           load_codes16_smem<BIN>(cq + off * BIN / 8, wv);
           const float s = decltype(scales_in_stage)::value
                               ? sq[off >> lgin]
-                              : ld_nc_f32(a.shard_scales(r0 + q) + ((e0 + off) >> lgin));
+                              : ld_nc_f32(v.shard_scales(r0 + q) + ((e0 + off) >> lgin));
           accumulate16<FIN, decltype(first)::value>(acc[j], wv, s, a.one);
         }
       };
@@ -672,21 +741,24 @@ __global__ void __launch_bounds__(kRedThreads, 2)
     __syncwarp();  // every lane has read the stage
     if (lane == 0) mbar_arrive(empty0 + 8 * st);
     if (k == nb - 1 && w < cnt) {  // last unit of the tile
-      if (a.sum_out) {
+      if (float *so = v.sums_out()) {
 #pragma unroll
         for (int j = 0; j < kU; ++j)
-          store16<DT_F32>(a.sum_out, e0 + j * kRun + lane * kVec, acc[j], a.wide != 0);
+          store16<DT_F32>(so, e0 + j * kRun + lane * kVec, acc[j], a.wide != 0);
       }
-      requant_tile<FOUT, kU, A>(a, acc, e0, lane);
+      requant_tile<FOUT, kU, RedView<A>>(v, acc, e0, lane);
     }
     if (++k == nb) {
       k = 0;
-      ct += gridDim.x;
+      for (ct += gridDim.x; ct >= nct && p < a.problems(); ct -= nct) ++p;
+      v.p = p;
     }
   }
-  // the partial last tile (fewer than 1024 elements) goes to warp 0 of CTA 0
+  // the partial last tile (fewer than 1024 elements) of every problem goes to
+  // warp 0 of CTA 0
   if ((a.n % kTile) != 0 && blockIdx.x == 0 && w == 0)
-    reduce_tail<FIN, FOUT, A>(a, nfull * kTile, lane);
+    for (int p = 0; p < a.problems(); ++p)
+      reduce_tail<FIN, FOUT, RedView<A>>(view_of(a, p), nfull * kTile, lane);
 }
 
 // ===========================================================================

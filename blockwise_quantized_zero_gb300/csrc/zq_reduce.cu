@@ -8,6 +8,14 @@
 
 namespace zq {
 
+// Elements of all the problems of one launch.
+static int64_t launch_elements(const ReduceArgs &a) { return a.n; }
+static int64_t launch_elements(const TableReduceArgs &a) { return a.n; }
+static int64_t launch_elements(const HopArgs &a) {
+  return ((a.n + kTile * kRedConsumers - 1) / (kTile * kRedConsumers)) * kTile * kRedConsumers *
+         a.nprob;
+}
+
 // Persistent grid of CTAs of eight consumer warps and one producer warp: one
 // CTA per CTA tile (8192 elements), at most one wave.
 template <int FIN, int FOUT, typename A> static cudaError_t go_r(const A &a, cudaStream_t st) {
@@ -16,7 +24,7 @@ template <int FIN, int FOUT, typename A> static cudaError_t go_r(const A &a, cud
   const int occ = ctas_per_sm<K, kSmem, kRedThreads>();
   if (occ < 1) return cudaErrorInvalidConfiguration;
   const int64_t span = int64_t(kRedConsumers) * kTile;
-  const int64_t ctas = (a.n + span - 1) / span;
+  const int64_t ctas = (launch_elements(a) + span - 1) / span;
   const int64_t cap = int64_t(device_sm_count()) * occ;
   const unsigned grid = static_cast<unsigned>(ctas < 1 ? 1 : (ctas < cap ? ctas : cap));
   return launch_pdl_threads(K, grid, kRedThreads, kSmem, st, a);
@@ -45,6 +53,10 @@ template <typename A> static cudaError_t go_r_io(const A &a, int fin, int fout, 
 }
 
 cudaError_t launch_reduce(const ReduceArgs &a, int fin, int fout, cudaStream_t st) {
+  return go_r_io(a, fin, fout, st);
+}
+
+cudaError_t launch_reduce_hop(const HopArgs &a, int fin, int fout, cudaStream_t st) {
   return go_r_io(a, fin, fout, st);
 }
 
