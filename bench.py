@@ -526,7 +526,7 @@ class QgzTwoHop:
     like qgz_reduce's shards). A step quantizes every gradient to int4 G=128
     with tensor-slice reordering, then runs the two-hop reduce: intra-node
     reduce + requantize to int4 G=128, inter-node reduce + requantize to int4
-    G=128 (2 x 8 reduce launches)."""
+    G=128 (two reduce launches, one per hop, each over all 8 GPUs' problems)."""
 
     name = "qgz_two_hop"
     dtype = "fp32 gradients in, int4 codes + fp32 scales between the hops and out"
@@ -584,8 +584,8 @@ class QgzTwoHop:
                               4 * n + packed_bytes(4, n, 128),
                               lambda g=g: zq.quantize_reordered(self.x[g], zq.INT4, 128, self.A,
                                                                 self.L, *self.q[g])))
-        out.append(Launch("two-hop reduce (2 x 8 launches, int4 G=128)", "reduce",
-                          self._reduce_bytes(), self.two_hop, kernels=2 * self.P))
+        out.append(Launch("two-hop reduce (one launch per hop, int4 G=128)", "reduce",
+                          self._reduce_bytes(), self.two_hop, kernels=2))
         return out
 
     def setup_e2e(self):
