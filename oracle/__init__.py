@@ -71,11 +71,20 @@ def _declare(lib):
     lib.orc_quantize_reordered.argtypes = [vp, i32, i64, i32, i64, i32, i32, vp, vp]
     lib.orc_reduce_two_hop.argtypes = [vp, vp, i32, i32, i64, i32, i64, vp, vp, i32, i64, vp, vp,
                                        i32, i64, vp]
+    lib.orc_il_bytes.argtypes = [i32, i64, i64]
+    lib.orc_il_bytes.restype = i64
+    lib.orc_quantize_interleaved.argtypes = [vp, i32, i64, i32, i64, vp]
+    lib.orc_dequantize_interleaved.argtypes = [vp, i64, i32, i64, vp, i32]
+    lib.orc_aquavit_bpw.argtypes = [i64, i64, ctypes.c_double, ctypes.c_double]
+    lib.orc_aquavit_bpw.restype = ctypes.c_double
+    lib.orc_aquavit_pick.argtypes = [ctypes.c_double, ctypes.POINTER(i32), ctypes.POINTER(i64)]
+    lib.orc_aquavit_pick.restype = ctypes.c_double
     lib.orc_encode_n.argtypes = [i32, vp, i64, vp]
     lib.orc_decode_n.argtypes = [i32, vp, i64, vp]
     lib.orc_encode_n.restype = i32
     lib.orc_decode_n.restype = i32
-    for name in ("orc_quantize", "orc_dequantize", "orc_reduce", "orc_fp8_accumulate"):
+    for name in ("orc_quantize", "orc_dequantize", "orc_reduce", "orc_fp8_accumulate",
+                 "orc_quantize_interleaved", "orc_dequantize_interleaved"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -168,6 +177,50 @@ def reduce(codes_list, scales_list, n: int, fmt_in: int, G_in: int, fmt_out: int
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return out_codes, out_scales, sum_out
+
+
+def il_bytes(fmt: int, n: int, G: int, lib=None) -> int:
+    """Bytes of the interleaved record stream (-1: no interleaved form)."""
+    return int((lib or load()).orc_il_bytes(fmt, n, G))
+
+
+def quantize_interleaved(x: np.ndarray, fmt: int, G: int, dtype: int | None = None,
+                         lib=None) -> np.ndarray:
+    """Return the record stream (uint8[il_bytes]): per block its fp32 scale, then its codes."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x)
+    n = x.size
+    nbytes = il_bytes(fmt, n, G, lib)
+    if nbytes < 0:
+        raise ValueError("oracle rejected the arguments")
+    rec = np.full(nbytes, GARBAGE, dtype=np.uint8)
+    if lib.orc_quantize_interleaved(_ptr(x), _dtype_code(x, dtype), n, fmt, G, _ptr(rec)) != 0:
+        raise ValueError("oracle rejected the arguments")
+    return rec
+
+
+def dequantize_interleaved(rec: np.ndarray, n: int, fmt: int, G: int, out_dtype: int,
+                           lib=None) -> np.ndarray:
+    """Dequantize a record stream (float32, or uint16 bit patterns for f16/bf16)."""
+    lib = lib or load()
+    rec = np.ascontiguousarray(rec, dtype=np.uint8)
+    out = np.full(n * np.dtype(_OUT_NP[out_dtype]).itemsize, GARBAGE, np.uint8).view(_OUT_NP[out_dtype])
+    if lib.orc_dequantize_interleaved(_ptr(rec), n, fmt, G, _ptr(out), out_dtype) != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out
+
+
+def aquavit_bpw(t: int, T: int, a: float = 0.9, c: float = 5.0, lib=None) -> float:
+    """Target width of the ascending schedule at step t of T."""
+    return float((lib or load()).orc_aquavit_bpw(t, T, a, c))
+
+
+def aquavit_pick(bpw: float, lib=None):
+    """(b, G, width) of the available pair nearest to a target width."""
+    lib = lib or load()
+    b, G = ctypes.c_int(0), ctypes.c_int64(0)
+    w = lib.orc_aquavit_pick(bpw, ctypes.byref(b), ctypes.byref(G))
+    return b.value, G.value, float(w)
 
 
 def slice_position(c: int, A: int, L: int) -> int:

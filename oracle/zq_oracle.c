@@ -66,6 +66,23 @@
  *      is one reduce as in R7.
  *  R12 the chunk size n / P is a multiple of 1024 elements, so every chunk
  *      is whole blocks and whole code words.
+ *  R13 [Aquavit]'s metadata interleaving (named in the summary of its
+ *      implementation, section 5.2-5.3; the layout itself is not described):
+ *      one byte stream of block records, record k = block k's fp32 scale (4
+ *      bytes, little endian) followed by block k's codes as their own bit
+ *      stream (R5) -- G*b/8 bytes for a whole block, the code bits of a
+ *      partial last block zero padded to whole 32-bit words. No padding
+ *      between records, so the stream is exactly as long as the planar codes
+ *      plus scales and the width stays b + 32/G bits per element. Integer
+ *      codes only (the b in {2,4,6,8} of granularity modulation).
+ *  R14 [Aquavit]'s ascending schedule (summary, Section 5.1): at step t of T
+ *      the target width is bpw(t) = 8 - 6/(a + c*t/T), (a, c) = (0.9, 5) by
+ *      default. The pages give the range of widths used, 2.03 (b = 2,
+ *      G = 1024) to 7.00 (b = 6, G = 32), and no rule that maps a width to a
+ *      (b, G) pair; the reading taken: the pair with b in {2,4,6} and G in
+ *      {32,...,1024} whose b + 32/G is nearest to bpw(t), ties to the
+ *      narrower. (The pages' mean of 5.79 bits over 1000 steps is not met by
+ *      this or by the continuous schedule, whose mean is 5.74.)
  */
 #include <math.h>
 #include <stddef.h>
@@ -523,4 +540,94 @@ int orc_decode_n(int kind, const uint32_t *c, int64_t n, float *out)
         else return ORC_BAD;
     }
     return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [Aquavit] metadata interleaving (reading R13)                            */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of the interleaved record stream of n elements, or -1 when the
+ * format has no interleaved form. */
+int64_t orc_il_bytes(int fmt, int64_t n, int64_t G)
+{
+    int64_t nb, k, total = 0;
+    if (fmt == ORC_E4M3 || !code_bits(fmt) || !valid_block(G) || n < 0) return -1;
+    nb = orc_num_blocks(n, G);
+    for (k = 0; k < nb; ++k) {
+        int64_t len = (n - k * G < G) ? n - k * G : G;
+        total += 4 + orc_codes_bytes(fmt, len);
+    }
+    return total;
+}
+
+/* Quantize n elements of src into the record stream rec (orc_il_bytes
+ * bytes): each block is quantized exactly as by orc_quantize, its scale
+ * written at the start of its record and its codes after it. */
+int orc_quantize_interleaved(const void *src, int dtype, int64_t n, int fmt, int64_t G, uint8_t *rec)
+{
+    int64_t k, i, nb, pos = 0;
+    if (orc_il_bytes(fmt, n, G) < 0 || !elem_size(dtype)) return ORC_BAD;
+    memset(rec, 0, (size_t)orc_il_bytes(fmt, n, G));
+    nb = orc_num_blocks(n, G);
+    for (k = 0; k < nb; ++k) {
+        int64_t lo = k * G, len = (n - lo < G) ? n - lo : G;
+        uint32_t sb;
+        float s;
+        for (i = 0; i < len; ++i) scratch[i] = load_elem(src, dtype, lo + i);
+        s = quantize_block(scratch, len, fmt, rec + pos + 4, 0);
+        sb = f32_to_bits(s);
+        for (i = 0; i < 4; ++i) rec[pos + i] = (uint8_t)(sb >> (8 * i));
+        pos += 4 + orc_codes_bytes(fmt, len);
+    }
+    return ORC_OK;
+}
+
+/* Dequantize a record stream: y = fl32(q * s) with s read from the record's
+ * head, then one RNE rounding to dst_dtype (as orc_dequantize). */
+int orc_dequantize_interleaved(const uint8_t *rec, int64_t n, int fmt, int64_t G, void *dst,
+                               int dst_dtype)
+{
+    int64_t k, i, nb, pos = 0;
+    if (orc_il_bytes(fmt, n, G) < 0 || !elem_size(dst_dtype)) return ORC_BAD;
+    nb = orc_num_blocks(n, G);
+    for (k = 0; k < nb; ++k) {
+        int64_t lo = k * G, len = (n - lo < G) ? n - lo : G;
+        uint32_t sb = 0;
+        float s;
+        for (i = 0; i < 4; ++i) sb |= (uint32_t)rec[pos + i] << (8 * i);
+        s = bits_to_f32(sb);
+        for (i = 0; i < len; ++i) store_elem(dst, dst_dtype, lo + i, dequant_elem(rec + pos + 4, s, fmt, i));
+        pos += 4 + orc_codes_bytes(fmt, len);
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [Aquavit] ascending schedule (reading R14)                               */
+/* ------------------------------------------------------------------------ */
+
+/* Target width at step t of T: 8 - 6 / (a + c t / T). */
+double orc_aquavit_bpw(int64_t t, int64_t T, double a, double c)
+{
+    return 8.0 - 6.0 / (a + c * (double)t / (double)T);
+}
+
+/* The (b, G) pair for a target width: nearest b + 32/G over b in {2,4,6},
+ * G in {32,...,1024}, ties to the narrower pair. Returns the pair's width. */
+double orc_aquavit_pick(double bpw, int *bits, int64_t *G)
+{
+    double best = -1.0, bestd = 0.0;
+    int b;
+    int64_t g;
+    for (b = 2; b <= 6; b += 2)
+        for (g = 32; g <= 1024; g *= 2) {
+            double w = b + 32.0 / (double)g, d = fabs(w - bpw);
+            if (best < 0.0 || d < bestd || (d == bestd && w < best)) {
+                best = w;
+                bestd = d;
+                *bits = b;
+                *G = g;
+            }
+        }
+    return best;
 }

@@ -672,6 +672,125 @@ def pin_two_hop_order(lib):
             assert np.all(sums[g] == np.float32(1.0)), (A, L, g)
 
 
+# ---------------------------------------------------------------------------
+# Aquavit: metadata interleaving and the ascending schedule ([Aquavit] summary
+# of the implementation, Section 5.1-5.3; Eq. 6; readings R13 and R14).
+# ---------------------------------------------------------------------------
+
+def _pack_lsb_first(q, bits):
+    """Two's-complement codes packed LSB first into 32-bit little-endian words
+    (an integer bit accumulator, independent of the oracle's bit writer)."""
+    acc, nbits = 0, 0
+    for v in q:
+        acc |= (int(v) & ((1 << bits) - 1)) << nbits
+        nbits += bits
+    nbytes = -(-nbits // 32) * 4
+    return acc.to_bytes(nbytes, "little")
+
+
+def pin_il_size(lib):
+    """The interleaved stream is exactly as long as codes plus scales: b + 32/G
+    bits per element (Eq. 6) for whole blocks; E4M3 has no interleaved form."""
+    fmt_of = {2: O.INT2, 4: O.INT4, 6: O.INT6, 8: O.INT8}
+    for b, fmt in fmt_of.items():
+        for G in BLOCKS:
+            for nblk in (1, 3, 64):
+                n = nblk * G
+                assert Fraction(O.il_bytes(fmt, n, G, lib) * 8, n) == b + Fraction(32, G), (b, G, n)
+    assert O.il_bytes(O.E4M3, 1024, 128, lib) == -1
+
+
+def pin_il_hand_records(lib):
+    """Two hand-built streams: records are [fp32 scale, little endian][codes]
+    with no padding; a partial last block's codes fill whole 32-bit words."""
+    import struct
+
+    # int4, G = 32, two blocks: block 0 holds k * 0.5 (absmax 3.5 -> scale 0.5,
+    # codes k exactly), block 1 is zero (scale 0, codes 0)
+    k = np.array([(i % 15) - 7 for i in range(32)])
+    x = np.concatenate([k * 0.5, np.zeros(32)]).astype(np.float32)
+    want = struct.pack("<f", 0.5) + _pack_lsb_first(k, 4) + struct.pack("<f", 0.0) + bytes(16)
+    got = O.quantize_interleaved(x, O.INT4, 32, lib=lib)
+    assert got.tobytes() == want, (got.tobytes().hex(), want.hex())
+    # 6-bit, G = 32, 40 elements: block 0 = k * 2^-3 (absmax 31/8 -> scale
+    # 1/8), block 1 = 8 elements (absmax 31/4 -> scale 1/4) -> 48 bits of codes
+    k0 = np.array([((3 * i) % 63) - 31 for i in range(32)])
+    k1 = np.array([31, -31, 1, 0, -1, 5, -6, 2])
+    x = np.concatenate([k0 / 8.0, k1 / 4.0]).astype(np.float32)
+    want = (struct.pack("<f", 0.125) + _pack_lsb_first(k0, 6) + struct.pack("<f", 0.25)
+            + _pack_lsb_first(k1, 6))
+    assert len(want) == 4 + 24 + 4 + 8
+    got = O.quantize_interleaved(x, O.INT6, 32, lib=lib)
+    assert got.tobytes() == want, (got.tobytes().hex(), want.hex())
+    y = O.dequantize_interleaved(got, x.size, O.INT6, 32, O.F32, lib=lib)
+    assert np.array_equal(y, x)
+
+
+def pin_il_is_a_regrouping(lib):
+    """Record k holds block k's planar scale and codes (the planar codec is
+    pinned above); dequantizing the stream gives the planar result."""
+    r = rng(31)
+    for fmt, G, n in ((O.INT2, 1024, 3 * 1024 + 200), (O.INT4, 128, 1000), (O.INT8, 32, 32 * 7 + 9)):
+        x = (r.standard_normal(n) * 0.02).astype(np.float32)
+        rec = O.quantize_interleaved(x, fmt, G, lib=lib).tobytes()
+        codes, scales = O.quantize(x, fmt, G, lib=lib)
+        pos = 0
+        for kb in range(-(-n // G)):
+            lo, hi = kb * G, min(n, kb * G + G)
+            cb = -(-(hi - lo) * O.BITS[fmt] // 32) * 4
+            assert rec[pos:pos + 4] == scales[kb:kb + 1].tobytes(), (fmt, G, kb)
+            start = lo * O.BITS[fmt] // 8
+            assert rec[pos + 4:pos + 4 + cb] == codes.tobytes()[start:start + cb], (fmt, G, kb)
+            pos += 4 + cb
+        assert pos == len(rec)
+        for dt in (O.F32, O.BF16):
+            y = O.dequantize_interleaved(np.frombuffer(rec, np.uint8), n, fmt, G, dt, lib=lib)
+            assert np.array_equal(y, O.dequantize(codes, scales, n, fmt, G, dt, lib=lib))
+
+
+def pin_schedule_closed_forms(lib):
+    """bpw(0) = 8 - 6/a and bpw(T) = 8 - 6/(a + c); the mean over t = 0..T-1
+    of an increasing function lies below its integral mean by at most
+    (f(T) - f(0))/T, and that integral mean is 8 - (6/c) ln((a + c)/a)."""
+    g = golden("aquavit_schedule.json")
+    for a, c, T in ((g["a"], g["c"], g["steps"]), (0.5, 2.0, 300), (1.5, 8.0, 64)):
+        f0, fT = O.aquavit_bpw(0, T, a, c, lib=lib), O.aquavit_bpw(T, T, a, c, lib=lib)
+        assert abs(f0 - (8 - 6 / a)) < 1e-12 and abs(fT - (8 - 6 / (a + c))) < 1e-12, (a, c)
+        mean = math.fsum(O.aquavit_bpw(t, T, a, c, lib=lib) for t in range(T)) / T
+        integral = 8 - (6 / c) * math.log((a + c) / a)
+        assert 0 <= integral - mean <= (fT - f0) / T + 1e-12, (a, c, T, mean, integral)
+        assert all(O.aquavit_bpw(t + 1, T, a, c, lib=lib) > O.aquavit_bpw(t, T, a, c, lib=lib)
+                   for t in range(T))
+
+
+def pin_schedule_pick(lib):
+    """The pairs: every available width maps to its own (b, G); the default
+    schedule starts at 2-bit/G=1024 and ends at 6-bit/G=32 as printed; no
+    pair wider than 7.00 is used; the pick is the nearest width (brute force
+    over the 18 pairs) and never decreases along the schedule."""
+    g = golden("aquavit_schedule.json")
+    pairs = [(b, G, b + Fraction(32, G)) for b in (2, 4, 6) for G in BLOCKS]
+    for b, G, w in pairs:
+        assert O.aquavit_pick(float(w), lib=lib)[:2] == (b, G), (b, G)
+    T, a, c = g["steps"], g["a"], g["c"]
+    first = O.aquavit_pick(O.aquavit_bpw(0, T, a, c, lib=lib), lib=lib)
+    last = O.aquavit_pick(O.aquavit_bpw(T, T, a, c, lib=lib), lib=lib)
+    assert (first[0], first[1], f"{first[2]:.2f}") == (g["first_pair"]["bits"], g["first_pair"]["G"],
+                                                       g["first_pair"]["bpw_printed"])
+    assert (last[0], last[1], f"{last[2]:.2f}") == (g["last_pair"]["bits"], g["last_pair"]["G"],
+                                                    g["last_pair"]["bpw_printed"])
+    assert O.aquavit_pick(8.5, lib=lib)[:2] == (6, 32) and O.aquavit_pick(0.0, lib=lib)[:2] == (2, 1024)
+    for target in np.linspace(1.0, 8.0, 701):
+        b, G, w = O.aquavit_pick(float(target), lib=lib)
+        best = min(abs(float(p[2]) - target) for p in pairs)
+        assert abs(w - target) == best and w == float(b + Fraction(32, G)), target
+    prev = 0.0
+    for t in range(T + 1):
+        w = O.aquavit_pick(O.aquavit_bpw(t, T, a, c, lib=lib), lib=lib)[2]
+        assert w >= prev
+        prev = w
+
+
 FAST_PINS = [
     pin_bpw_endpoints, pin_bpw_formula, pin_zeropp_payload, pin_bit_layout,
     pin_e4m3_points, pin_e4m3_vs_library, pin_f16_vs_library, pin_bf16_vs_library,
@@ -681,5 +800,6 @@ FAST_PINS = [
     pin_reduce_order, pin_reduce_plain_sum_and_bound, pin_reduce_two_roundings,
     pin_fp8_reduce_no_overflow, pin_fp8_accumulate, pin_fp8_accumulate_two_roundings,
     pin_reordered_quantize_identity, pin_two_hop_ownership, pin_two_hop_exact_sums,
-    pin_two_hop_order,
+    pin_two_hop_order, pin_il_size, pin_il_hand_records, pin_il_is_a_regrouping,
+    pin_schedule_closed_forms, pin_schedule_pick,
 ]

@@ -78,6 +78,29 @@ MUTANTS = [
      "                            out_scales[a * L + l], fmt_out, G_out, sums ? sums[a * L + l] : 0);",
      "            rc = orc_reduce(sc, ss, A, m, fmt_mid, G_mid, out_codes[l * A + a],\n"
      "                            out_scales[l * A + a], fmt_out, G_out, sums ? sums[l * A + a] : 0);"),
+    ("il_scale_big_endian", "for (i = 0; i < 4; ++i) rec[pos + i] = (uint8_t)(sb >> (8 * i));",
+     "for (i = 0; i < 4; ++i) rec[pos + i] = (uint8_t)(sb >> (8 * (3 - i)));"),
+    ("il_codes_before_scale",
+     "s = quantize_block(scratch, len, fmt, rec + pos + 4, 0);\n"
+     "        sb = f32_to_bits(s);\n"
+     "        for (i = 0; i < 4; ++i) rec[pos + i] = (uint8_t)(sb >> (8 * i));",
+     "s = quantize_block(scratch, len, fmt, rec + pos, 0);\n"
+     "        sb = f32_to_bits(s);\n"
+     "        for (i = 0; i < 4; ++i) rec[pos + orc_codes_bytes(fmt, len) + i] = (uint8_t)(sb >> (8 * i));"),
+    # (stays inside the buffer: records overlap instead of running past its end)
+    ("il_stride_without_scale",
+     "        pos += 4 + orc_codes_bytes(fmt, len);\n    }\n    return ORC_OK;\n}\n\n/* Dequantize a record stream",
+     "        pos += orc_codes_bytes(fmt, len);\n    }\n    return ORC_OK;\n}\n\n/* Dequantize a record stream"),
+    ("il_dequant_reads_codes_as_scale", "for (i = 0; i < 4; ++i) sb |= (uint32_t)rec[pos + i] << (8 * i);",
+     "for (i = 0; i < 4; ++i) sb |= (uint32_t)rec[pos + 4 + i] << (8 * i);"),
+    ("il_size_without_scales", "total += 4 + orc_codes_bytes(fmt, len);", "total += orc_codes_bytes(fmt, len);"),
+    ("schedule_a_c_swapped", "return 8.0 - 6.0 / (a + c * (double)t / (double)T);",
+     "return 8.0 - 6.0 / (c + a * (double)t / (double)T);"),
+    ("schedule_descending", "return 8.0 - 6.0 / (a + c * (double)t / (double)T);",
+     "return 8.0 - 6.0 / (a + c * (double)(T - t) / (double)T);"),
+    ("pick_rounds_up", "double w = b + 32.0 / (double)g, d = fabs(w - bpw);",
+     "double w = b + 32.0 / (double)g, d = (w >= bpw) ? w - bpw : 1e9;"),
+    ("pick_allows_8_bit", "for (b = 2; b <= 6; b += 2)", "for (b = 2; b <= 8; b += 2)"),
 ]
 
 
