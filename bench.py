@@ -871,8 +871,161 @@ class Llama70B:
                              "G=32 round trips, single thread")
 
 
+class AquavitSchedule:
+    """Aquavit's weight codec over its ascending schedule: bpw(t) = 8 -
+    6/(a + c t/T) with (a, c) = (0.9, 5) and T = 1000 steps, each step's width
+    mapped to the nearest available b + 32/G (b in {2,4,6}). A benchmark step
+    is one whole schedule on the 8192x8192 bf16 weight shard (N(0, 0.02),
+    seed 2): every schedule step quantizes the shard at its (b, G) and
+    dequantizes it to bf16, once in the metadata-interleaved record layout and
+    once in the planar layout, so the two layouts compare on the same calls.
+    Calls rotate over 8 buffer sets (no call finds its inputs in L2)."""
+
+    name = "aquavit_schedule"
+    dtype = "bf16 in, int2/4/6 codes + fp32 scales (interleaved records or planar), bf16 out"
+    rows, cols = 8192, 8192
+    T, a, c = 1000, 0.9, 5.0
+    slots = 8
+
+    def __init__(self):
+        from blockwise_quantized_zero_gb300 import inputs
+
+        self.n = self.rows * self.cols
+        self.host = inputs.weight_shard_bf16(self.rows, self.cols)
+
+    def config(self):
+        return {"workload": "aquavit_schedule: one 8192x8192 bf16 weight shard (N(0,0.02)); the "
+                            "1000-step ascending schedule bpw = 8 - 6/(0.9 + 5 t/1000), each step "
+                            "quantize + dequantize->bf16 at its nearest (b, G); interleaved "
+                            "records and planar layout, each for the whole schedule",
+                "elements": self.n, "schedule_steps": self.T, "a": self.a, "c": self.c,
+                "pairs": {f"{b}:{G}": k for (b, G), k in sorted(self.counts.items())}
+                if hasattr(self, "counts") else None,
+                "mean_bpw": getattr(self, "mean_bpw", None),
+                "l2": "no flush: calls rotate over 8 buffer sets of 134 MB source + output each"}
+
+    def setup(self):
+        import torch
+
+        import blockwise_quantized_zero_gb300 as zq
+
+        self.zq = zq
+        counts = {}
+        width = 0.0
+        for t in range(self.T):
+            fmt, G, _, w = zq.aquavit_schedule(t, self.T, self.a, self.c)
+            counts[(fmt, G)] = counts.get((fmt, G), 0) + 1
+            width += w
+        self.counts, self.mean_bpw = counts, round(width / self.T, 5)
+        n, S = self.n, self.slots
+        src0 = _dev_bf16(self.host)
+        self.src = [src0] + [src0.clone() for _ in range(S - 1)]
+        rmax = max(zq.interleaved_bytes(b, n, G) for b, G in counts)
+        self.rec = [torch.empty(rmax, dtype=torch.uint8, device="cuda") for _ in range(S)]
+        self.codes = [torch.empty(zq.codes_bytes(6, n), dtype=torch.uint8, device="cuda")
+                      for _ in range(S)]
+        self.scales = [torch.empty(zq.num_blocks(n, 32), dtype=torch.float32, device="cuda")
+                       for _ in range(S)]
+        self.out = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(S)]
+
+    def _calls(self, k, body):
+        def run():
+            for j in range(k):
+                body(j % self.slots)
+        return run
+
+    def launches(self):
+        zq, n = self.zq, self.n
+        out = []
+        for (b, G), k in sorted(self.counts.items()):
+            nb = 2 * n + packed_bytes(b, n, G)
+            rb, cb, sb = zq.interleaved_bytes(b, n, G), zq.codes_bytes(b, n), zq.num_blocks(n, G)
+            out.append(Launch(f"quantize_il bf16 {fmt_name(b)} G={G} x{k}", "quantize_il", k * nb,
+                              self._calls(k, lambda i, b=b, G=G, rb=rb: zq.quantize_interleaved(
+                                  self.src[i], b, G, self.rec[i][:rb])), kernels=k))
+            out.append(Launch(f"dequantize_il {fmt_name(b)} G={G} bf16 x{k}", "dequantize_il",
+                              k * nb, self._calls(k, lambda i, b=b, G=G, rb=rb:
+                                                  zq.dequantize_interleaved(
+                                                      self.rec[i][:rb], n, b, G, out=self.out[i])),
+                              kernels=k))
+            out.append(Launch(f"quantize bf16 {fmt_name(b)} G={G} x{k}", "quantize", k * nb,
+                              self._calls(k, lambda i, b=b, G=G, cb=cb, sb=sb: zq.quantize(
+                                  self.src[i], b, G, self.codes[i][:cb], self.scales[i][:sb])),
+                              kernels=k))
+            out.append(Launch(f"dequantize {fmt_name(b)} G={G} bf16 x{k}", "dequantize", k * nb,
+                              self._calls(k, lambda i, b=b, G=G, cb=cb, sb=sb: zq.dequantize(
+                                  self.codes[i][:cb], self.scales[i][:sb], n, b, G,
+                                  out=self.out[i])), kernels=k))
+        return out
+
+    def step_bytes(self):
+        return sum(2 * 2 * k * (2 * self.n + packed_bytes(b, self.n, G))
+                   for (b, G), k in self.counts.items())
+
+    # end to end: each of the 18 pairs once, interleaved records through host memory
+    def setup_e2e(self):
+        import torch
+
+        zq, n = self.zq, self.n
+        self.h_src = torch.from_numpy(self.host.view(np.int16)).view(torch.bfloat16).pin_memory()
+        rmax = self.rec[0].numel()
+
+        def make_set():
+            dev = dict(device="cuda")
+            return dict(h_rec=torch.empty(rmax, dtype=torch.uint8).pin_memory(),
+                        h_out=torch.empty(n, dtype=torch.bfloat16).pin_memory(),
+                        d_src=torch.empty(n, dtype=torch.bfloat16, **dev),
+                        d_rec=torch.empty(rmax, dtype=torch.uint8, **dev),
+                        d_rec2=torch.empty(rmax, dtype=torch.uint8, **dev),
+                        d_out=torch.empty(n, dtype=torch.bfloat16, **dev))
+
+        self.fork = ForkedStreams(make_set)
+        h2d = sum(2 * n + zq.interleaved_bytes(b, n, G) for b, G in self.counts)
+        d2h = sum(zq.interleaved_bytes(b, n, G) + 2 * n for b, G in self.counts)
+        return h2d, d2h
+
+    def e2e_step(self):
+        """Per pair: host src -> quantize_interleaved -> host records; host
+        records -> dequantize_interleaved -> host out (pairs alternate between
+        two streams)."""
+        zq, n = self.zq, self.n
+
+        def one(pair, B):
+            b, G = pair
+            rb = zq.interleaved_bytes(b, n, G)
+            B["d_src"].copy_(self.h_src, non_blocking=True)
+            zq.quantize_interleaved(B["d_src"], b, G, B["d_rec"][:rb])
+            B["h_rec"][:rb].copy_(B["d_rec"][:rb], non_blocking=True)
+            B["d_rec2"][:rb].copy_(B["h_rec"][:rb], non_blocking=True)
+            zq.dequantize_interleaved(B["d_rec2"][:rb], n, b, G, out=B["d_out"])
+            B["h_out"].copy_(B["d_out"], non_blocking=True)
+
+        self.fork.run(sorted(self.counts), one)
+
+    def e2e_bytes(self):
+        return sum(2 * (2 * self.n + packed_bytes(b, self.n, G)) for b, G in self.counts)
+
+    def oracle_sample(self, sample=1 << 22):
+        import oracle as O
+
+        x = np.ascontiguousarray(self.host[:sample])
+        pairs = sorted({O.aquavit_pick(O.aquavit_bpw(t, self.T, self.a, self.c))[:2]
+                        for t in range(self.T)})
+
+        def run():
+            for b, G in pairs:
+                rec = O.quantize_interleaved(x, b, G, dtype=O.BF16)
+                O.dequantize_interleaved(rec, sample, b, G, O.BF16)
+
+        nbytes = sum(2 * (2 * sample + packed_bytes(b, sample, G)) for b, G in pairs)
+        desc = (f"first {sample:,} elements of the shard, each of the schedule's {len(pairs)} "
+                "(b, G) pairs once, interleaved quantize + dequantize->bf16, single thread")
+        return run, nbytes, desc
+
+
 WORKLOADS = {"gm_sweep": GMSweep, "qwz_fp16": QwzFP16, "qgz_reduce": QgzReduce,
-             "agoq_fp8": AgoqFP8, "llama70b": Llama70B, "qgz_two_hop": QgzTwoHop}
+             "agoq_fp8": AgoqFP8, "llama70b": Llama70B, "qgz_two_hop": QgzTwoHop,
+             "aquavit_schedule": AquavitSchedule}
 
 
 # ---------------------------------------------------------------------------

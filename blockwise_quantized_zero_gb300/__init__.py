@@ -61,6 +61,16 @@ def _declare(L):
     L.zq_fp8_accumulate.argtypes = [vp, vp, vp, i32, i64, i64, vp]
     for f in ("zq_quantize", "zq_dequantize", "zq_reduce_quantized", "zq_fp8_accumulate"):
         getattr(L, f).restype = i32
+    L.zq_interleaved_bytes.argtypes = [i32, i64, i64]
+    L.zq_interleaved_bytes.restype = sz
+    L.zq_quantize_interleaved.argtypes = [vp, i32, i64, i32, i64, vp, vp]
+    L.zq_quantize_interleaved.restype = i32
+    L.zq_dequantize_interleaved.argtypes = [vp, i64, i32, i64, vp, i32, vp]
+    L.zq_dequantize_interleaved.restype = i32
+    L.zq_aquavit_schedule.argtypes = [i64, i64, ctypes.c_double, ctypes.c_double,
+                                      ctypes.POINTER(i32), ctypes.POINTER(i64),
+                                      ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+    L.zq_aquavit_schedule.restype = i32
     L.zq_status_string.argtypes = [i32]
     L.zq_status_string.restype = ctypes.c_char_p
     L.zq_last_cuda_error.argtypes = []
@@ -166,6 +176,48 @@ def dequantize(codes, scales, n: int, fmt: int, G: int, out_dtype=None, out=None
     _check(lib().zq_dequantize(codes.data_ptr(), scales.data_ptr(), n, fmt, G, out.data_ptr(),
                                dtype_code(out.dtype), _stream(codes, stream)), "zq_dequantize")
     return out
+
+
+def interleaved_bytes(fmt: int, n: int, G: int) -> int:
+    """Bytes of the metadata-interleaved record stream (0: integer formats only)."""
+    return int(lib().zq_interleaved_bytes(fmt, n, G))
+
+
+def quantize_interleaved(src, fmt: int, G: int, records=None, stream=None):
+    """Quantize a CUDA tensor into one uint8 stream of block records (fp32 scale, then codes)."""
+    torch = _torch()
+    _cuda_contig(src, "src")
+    n = src.numel()
+    if records is None:
+        records = torch.empty(max(interleaved_bytes(fmt, n, G), 1), dtype=torch.uint8,
+                              device=src.device)
+    _check(lib().zq_quantize_interleaved(src.data_ptr(), dtype_code(src.dtype), n, fmt, G,
+                                         records.data_ptr(), _stream(src, stream)),
+           "zq_quantize_interleaved")
+    return records
+
+
+def dequantize_interleaved(records, n: int, fmt: int, G: int, out_dtype=None, out=None,
+                           stream=None):
+    """Dequantize a record stream -> a CUDA tensor of n elements (default bf16)."""
+    torch = _torch()
+    _cuda_contig(records, "records")
+    if out is None:
+        out = torch.empty(n, dtype=out_dtype or torch.bfloat16, device=records.device)
+    _check(lib().zq_dequantize_interleaved(records.data_ptr(), n, fmt, G, out.data_ptr(),
+                                           dtype_code(out.dtype), _stream(records, stream)),
+           "zq_dequantize_interleaved")
+    return out
+
+
+def aquavit_schedule(t: int, T: int, a: float = 0.9, c: float = 5.0):
+    """(format, G, target width, pair width) of the ascending schedule at step t of T."""
+    fmt, G = ctypes.c_int(0), ctypes.c_int64(0)
+    want, width = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    _check(lib().zq_aquavit_schedule(t, T, a, c, ctypes.byref(fmt), ctypes.byref(G),
+                                     ctypes.byref(want), ctypes.byref(width)),
+           "zq_aquavit_schedule")
+    return fmt.value, G.value, want.value, width.value
 
 
 def _reduce(entry: str, codes_list, scales_list, n, fmt_in, G_in, fmt_out, G_out, out_codes,

@@ -3,6 +3,7 @@
 // units. Every argument error is reported before any work is enqueued.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -346,6 +347,71 @@ zq_status zq_reduce_two_hop(const void *const *codes, const float *const *scales
   h.L = L;
   h.bits_in = bmid;
   if (zq_status s2 = from_cuda(launch_reduce_hop(h, format_mid, format_out, st))) return s2;
+  return ZQ_OK;
+}
+
+size_t zq_interleaved_bytes(int format, int64_t n, int64_t G) {
+  if (format == ZQ_E4M3 || !bits_of(format) || n < 0 || !valid_block(G)) return 0;
+  return zq_codes_bytes(format, n) + size_t(zq_num_blocks(n, G)) * 4u;
+}
+
+zq_status zq_quantize_interleaved(const void *src, int src_dtype, int64_t n, int format, int64_t G,
+                                  void *records, void *stream) {
+  if (format == ZQ_E4M3 || !bits_of(format) || !elem_bytes(src_dtype)) return ZQ_ERR_UNSUPPORTED;
+  if (n < 0 || !valid_block(G)) return ZQ_ERR_INVALID_ARG;
+  if (n == 0) return ZQ_OK;
+  if (!src || !records) return ZQ_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(records)) return ZQ_ERR_MISALIGNED;
+  const Range rs(src, size_t(n) * elem_bytes(src_dtype)),
+      rr(records, zq_interleaved_bytes(format, n, G));
+  if (rr.overlaps(rs)) return ZQ_ERR_ALIAS;
+  for (const void *p : {src, static_cast<const void *>(records)})
+    if (zq_status st = check_device_ptr(p)) return st;
+  return from_cuda(launch_quantize_interleaved(src, src_dtype, n, format, G, records,
+                                               as_stream(stream), aligned32(src)));
+}
+
+zq_status zq_dequantize_interleaved(const void *records, int64_t n, int format, int64_t G,
+                                    void *dst, int dst_dtype, void *stream) {
+  if (format == ZQ_E4M3 || !bits_of(format) || !elem_bytes(dst_dtype)) return ZQ_ERR_UNSUPPORTED;
+  if (n < 0 || !valid_block(G)) return ZQ_ERR_INVALID_ARG;
+  if (n == 0) return ZQ_OK;
+  if (!records || !dst) return ZQ_ERR_INVALID_ARG;
+  if (!aligned16(records) || !aligned16(dst)) return ZQ_ERR_MISALIGNED;
+  const Range rd(dst, size_t(n) * elem_bytes(dst_dtype)),
+      rr(records, zq_interleaved_bytes(format, n, G));
+  if (rd.overlaps(rr)) return ZQ_ERR_ALIAS;
+  for (const void *p : {records, static_cast<const void *>(dst)})
+    if (zq_status st = check_device_ptr(p)) return st;
+  return from_cuda(launch_dequantize_interleaved(records, n, format, G, dst, dst_dtype,
+                                                 as_stream(stream), aligned32(dst)));
+}
+
+zq_status zq_aquavit_schedule(int64_t t, int64_t T, double a, double c, int *format, int64_t *G,
+                              double *target, double *width) {
+  if (!format || !G || T < 1 || t < 0 || t > T || !(a > 0.0) || !(c >= 0.0) || !std::isfinite(a) ||
+      !std::isfinite(c))
+    return ZQ_ERR_INVALID_ARG;
+  const double want = 8.0 - 6.0 / (a + c * double(t) / double(T));
+  // The 18 available widths in increasing order (b = 2, 4, 6; G = 1024 .. 32);
+  // scanning upwards with a strict comparison keeps the narrower pair on a tie.
+  int best_b = 0;
+  int64_t best_G = 0;
+  double best_w = 0.0, best_d = 0.0;
+  for (int b = 2; b <= 6; b += 2)
+    for (int64_t g = 1024; g >= 32; g /= 2) {
+      const double w = double(b) + 32.0 / double(g), d = std::fabs(w - want);
+      if (best_b == 0 || d < best_d) {
+        best_b = b;
+        best_G = g;
+        best_w = w;
+        best_d = d;
+      }
+    }
+  *format = best_b;  // ZQ_INT2 / ZQ_INT4 / ZQ_INT6 are the bit counts
+  *G = best_G;
+  if (target) *target = want;
+  if (width) *width = best_w;
   return ZQ_OK;
 }
 

@@ -76,6 +76,11 @@ cudaError_t launch_quantize(const void *src, int dt, int64_t n, int fmt, int64_t
                             const SliceRemap &rm = SliceRemap{1, 1, 0});
 cudaError_t launch_dequantize(const void *codes, const float *scales, int64_t n, int fmt,
                               int64_t G, void *dst, int dt, cudaStream_t st, bool wide);
+// The metadata-interleaved record layout (integer codes).
+cudaError_t launch_quantize_interleaved(const void *src, int dt, int64_t n, int fmt, int64_t G,
+                                        void *rec, cudaStream_t st, bool wide);
+cudaError_t launch_dequantize_interleaved(const void *rec, int64_t n, int fmt, int64_t G, void *dst,
+                                          int dt, cudaStream_t st, bool wide);
 cudaError_t launch_reduce(const ReduceArgs &a, int fin, int fout, cudaStream_t st);
 // All P reduces of one hop of the two-hop reduce in one launch.
 cudaError_t launch_reduce_hop(const HopArgs &a, int fin, int fout, cudaStream_t st);

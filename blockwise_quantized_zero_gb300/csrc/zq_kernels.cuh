@@ -22,6 +22,45 @@ constexpr int kU = 2;                      // 16-element runs per lane per tile
 constexpr int kTile = 32 * kVec * kU;      // 1024 elements per warp tile
 constexpr int kRun = 32 * kVec;            // 512 elements per warp-wide run
 
+// ---------------------------------------------------------------------------
+// Layouts of the quantized form. Planar: the codes are one LSB-first bit
+// stream and the block scales a separate fp32 array. Interleaved (Aquavit's
+// metadata interleaving): one byte stream of block records, record k = block
+// k's fp32 scale followed by its codes (G*b/8 bytes), so the record stride
+// 4 + G*b/8 is a multiple of 4 bytes but not of 8; integer codes only. The
+// quantize and dequantize kernels take the layout as a template flag IL.
+// ---------------------------------------------------------------------------
+__host__ __device__ constexpr int log2_of(int G) { return G <= 1 ? 0 : 1 + log2_of(G / 2); }
+
+template <int B> __device__ __forceinline__ int64_t il_stride(int lg) {
+  return 4 + ((int64_t(B) << lg) >> 3);
+}
+
+// Byte offset of the code bits of element e, e the first element of a
+// 16-element run or of a block (blocks of 2^lg elements).
+template <bool IL, int B> __device__ __forceinline__ int64_t code_off(int64_t e, int lg) {
+  if constexpr (IL) {
+    const int64_t k = e >> lg;
+    return k * il_stride<B>(lg) + 4 + (((e - (k << lg)) * B) >> 3);
+  } else {
+    return e * B / 8;
+  }
+}
+
+template <bool IL, int B>
+__device__ __forceinline__ void put_codes16(uint8_t *p, const uint32_t (&w)[B / 2]) {
+  if constexpr (IL) store_codes16_a4<B>(p, w);
+  else store_codes16<B>(p, w);
+}
+
+// Store the scale of block k (blocks of 2^lg elements).
+template <bool IL, int B>
+__device__ __forceinline__ void put_scale(uint8_t *codes, float *scales, int64_t k, int lg,
+                                          float s) {
+  if constexpr (IL) *reinterpret_cast<float *>(codes + k * il_stride<B>(lg)) = s;
+  else scales[k] = s;
+}
+
 // Programmatic dependent launch: wait until the previous grid on the stream
 // has completed and its writes are visible, then let the next grid be
 // scheduled. Every kernel calls this before its first global memory access.
@@ -71,14 +110,16 @@ struct SliceRemap {
 // its reciprocal for block l of the tile (there are 1024 / G <= 32 blocks),
 // stores it, and the values are shuffled back to the lanes of each block.
 // m[j] is the lane's block absmax for run j (already reduced over the block).
-template <int FMT, int G>
+template <int FMT, int G, bool IL>
 __device__ __forceinline__ void tile_scales(const float (&m)[kU], float (&s)[kU], float (&r)[kU],
+                                            uint8_t *__restrict__ codes,
                                             float *__restrict__ scales, int64_t e0, int lane) {
+  constexpr int B = Fmt<FMT>::kBits, LG = log2_of(G);
   if constexpr (G == kTile) {
     const float sb = block_scale<FMT>(fmaxf(m[0], m[1])), rb = safe_rcp(sb);
     s[0] = s[1] = sb;
     r[0] = r[1] = rb;
-    if (lane == 0) scales[e0 / G] = sb;
+    if (lane == 0) put_scale<IL, B>(codes, scales, e0 / G, LG, sb);
   } else {
     constexpr int L = G / kVec;          // lanes per block
     constexpr int PER_RUN = kRun / G;    // blocks per run
@@ -88,7 +129,7 @@ __device__ __forceinline__ void tile_scales(const float (&m)[kU], float (&s)[kU]
     const float g0 = __shfl_sync(kFull, m[0], src), g1 = __shfl_sync(kFull, m[1], src);
     const float mb = (lane < PER_RUN) ? g0 : g1;
     const float sb = block_scale<FMT>(mb), rb = safe_rcp(sb);
-    if (lane < NB) scales[e0 / G + lane] = sb;
+    if (lane < NB) put_scale<IL, B>(codes, scales, e0 / G + lane, LG, sb);
     // scatter: the lanes of block (j, lane / L) fetch its scale
 #pragma unroll
     for (int j = 0; j < kU; ++j) {
@@ -119,7 +160,7 @@ template <int DT> struct FixQueue {
 // Fix the queued runs [first, first + count) of warp w: lane i takes entry
 // first + i, recomputes its 16 codes with the exact resolution of the
 // flagged elements, and overwrites the fast-path code words.
-template <int DT, int FMT, int G>
+template <int DT, int FMT, int G, bool IL>
 __device__ __noinline__ void quantize_flush(FixQueue<DT> &fq, int w, int first, int count,
                                             const void *__restrict__ src,
                                             uint8_t *__restrict__ codes, int lane, bool wide,
@@ -142,7 +183,7 @@ __device__ __noinline__ void quantize_flush(FixQueue<DT> &fq, int w, int first, 
       float x[kVec];
       widen16<DT>(raw, x);
       const float r = safe_rcp(s);
-      uint8_t *cp = codes + e * B / 8;
+      uint8_t *cp = codes + code_off<IL, B>(e, log2_of(G));
       uint32_t wd[W];
       const bool normal = (FMT == F_E4M3) ? scale_is_normal(s) : (s == 0.0f || scale_is_normal(s));
       if (normal && FMT != F_E4M3) {
@@ -153,13 +194,13 @@ __device__ __noinline__ void quantize_flush(FixQueue<DT> &fq, int w, int first, 
       } else {
         quant16_exact<FMT>(x, s, wd);
       }
-      store_codes16<B>(cp, wd);
+      put_codes16<IL, B>(cp, wd);
     }
   }
   __syncwarp();
 }
 
-template <int DT, int FMT, int G>
+template <int DT, int FMT, int G, bool IL>
 __device__ __forceinline__ void quantize_tile(const uint32_t (&raw)[kU][kRawWords<DT>],
                                               uint8_t *__restrict__ codes,
                                               float *__restrict__ scales, int64_t e0, int lane,
@@ -179,14 +220,14 @@ __device__ __forceinline__ void quantize_tile(const uint32_t (&raw)[kU][kRawWord
     m[0] = m[1] = warp_max(fmaxf(m[0], m[1]));
   }
   float s[kU], r[kU];
-  tile_scales<FMT, G>(m, s, r, scales, e0, lane);
+  tile_scales<FMT, G, IL>(m, s, r, codes, scales, e0, lane);
 
 #pragma unroll
   for (int j = 0; j < kU; ++j) {
     uint32_t wd[W];
     const int64_t e = e0 + j * kRun + lane * kVec;
     const uint32_t flagged = quant16_try_fast<FMT>(x[j], s[j], r[j], wd);
-    store_codes16<B>(codes + e * B / 8, wd);
+    put_codes16<IL, B>(codes + code_off<IL, B>(e, log2_of(G)), wd);
     const unsigned ballot = __ballot_sync(kFull, flagged != 0u);
     if (ballot) {
       if (flagged) {
@@ -205,20 +246,20 @@ __device__ __forceinline__ void quantize_tile(const uint32_t (&raw)[kU][kRawWord
 
 // Exact, warp-cooperative quantization of elements [e0, n) (fewer than one
 // tile; e0 is a multiple of G). Each lane builds whole 32-bit code words.
-template <int DT, int FMT, int G>
+template <int DT, int FMT, int G, bool IL>
 __device__ __noinline__ void quantize_tail(const void *__restrict__ src,
                                            uint8_t *__restrict__ codes,
                                            float *__restrict__ scales, int64_t e0, int64_t n,
                                            int lane) {
   constexpr int B = Fmt<FMT>::kBits;
-  uint32_t *cw = reinterpret_cast<uint32_t *>(codes);
   for (int64_t lo = e0; lo < n; lo += G) {
+    uint32_t *cw = reinterpret_cast<uint32_t *>(codes + code_off<IL, B>(lo, log2_of(G)));
     const int64_t hi = (lo + G < n) ? lo + G : n;
     float m = 0.0f;
     for (int64_t i = lo + lane; i < hi; i += 32) m = fmaxf(m, fabsf(load1_f32<DT>(src, i)));
     const float s = block_scale<FMT>(warp_max(m));
-    if (lane == 0) scales[lo / G] = s;
-    const int64_t len = hi - lo, nwords = (len * B + 31) / 32, w0 = lo * B / 32;
+    if (lane == 0) put_scale<IL, B>(codes, scales, lo / G, log2_of(G), s);
+    const int64_t len = hi - lo, nwords = (len * B + 31) / 32;
     for (int64_t wi = lane; wi < nwords; wi += 32) {
       const int64_t bit0 = wi * 32;
       const int64_t first = bit0 / B;
@@ -229,17 +270,18 @@ __device__ __noinline__ void quantize_tail(const void *__restrict__ src,
         const int sh = static_cast<int>(e * B - bit0);
         word |= (sh >= 0) ? (c << sh) : (c >> (-sh));
       }
-      cw[w0 + wi] = word;
+      cw[wi] = word;
     }
   }
 }
 
-template <int DT, int FMT, int G>
+template <int DT, int FMT, int G, bool IL = false>
 __global__ void __launch_bounds__(kThreads, 3) quantize_kernel(const void *__restrict__ src,
                                                             uint8_t *__restrict__ codes,
                                                             float *__restrict__ scales,
                                                             int64_t n, int wide,
                                                             const SliceRemap rm) {
+  static_assert(!IL || FMT != F_E4M3, "the interleaved layout holds integer codes");
   const WarpCursor c;
   const int64_t nfull = n / kTile;
   const bool wd = wide != 0;
@@ -266,14 +308,14 @@ __global__ void __launch_bounds__(kThreads, 3) quantize_kernel(const void *__res
       for (int j = 0; j < kU; ++j)
         load16_raw<DT>(src, tn * kTile + j * kRun + c.lane * kVec, raw[j], wd);
     }
-    quantize_tile<DT, FMT, G>(cur, codes, scales, rm.out_tile(t) * kTile, c.lane, fq, w, count);
+    quantize_tile<DT, FMT, G, IL>(cur, codes, scales, rm.out_tile(t) * kTile, c.lane, fq, w, count);
     while (count >= 32) {  // fix full batches right away, newest first
       count -= 32;
-      quantize_flush<DT, FMT, G>(fq, w, count, 32, src, codes, c.lane, wd, rm);
+      quantize_flush<DT, FMT, G, IL>(fq, w, count, 32, src, codes, c.lane, wd, rm);
     }
   }
-  if (count) quantize_flush<DT, FMT, G>(fq, w, 0, count, src, codes, c.lane, wd, rm);
-  if (c.owns_tail(n)) quantize_tail<DT, FMT, G>(src, codes, scales, nfull * kTile, n, c.lane);
+  if (count) quantize_flush<DT, FMT, G, IL>(fq, w, 0, count, src, codes, c.lane, wd, rm);
+  if (c.owns_tail(n)) quantize_tail<DT, FMT, G, IL>(src, codes, scales, nfull * kTile, n, c.lane);
 }
 
 // ===========================================================================
@@ -283,12 +325,13 @@ __global__ void __launch_bounds__(kThreads, 3) quantize_kernel(const void *__res
 // (whose larger register slots would otherwise cost occupancy).
 template <int FMT> constexpr int kDequantAhead = Fmt<FMT>::kBits <= 4 ? 6 : 4;
 
-template <int FMT, int DT>
+template <int FMT, int DT, bool IL = false>
 __global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t *__restrict__ codes,
                                                               const float *__restrict__ scales,
                                                               void *__restrict__ dst, int64_t n,
                                                               int log2G, int wide) {
   constexpr int B = Fmt<FMT>::kBits, W = Fmt<FMT>::kWords16;
+  static_assert(!IL || FMT != F_E4M3, "the interleaved layout holds integer codes");
   const WarpCursor c;
   const int64_t nfull = n / kTile;
   const bool wd = wide != 0;
@@ -302,8 +345,15 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t *__r
 #pragma unroll
     for (int j = 0; j < kU; ++j) {
       const int64_t e = tile * kTile + j * kRun + c.lane * kVec;
-      load_codes16<B>(codes + e * B / 8, wd_[j]);
-      sd_[j] = ld_nc_f32(scales + (e >> log2G));
+      if constexpr (IL) {  // the run's record: scale, then codes
+        const int64_t k = e >> log2G;
+        const uint8_t *rec = codes + k * il_stride<B>(log2G);
+        load_codes16_a4<B>(rec + 4 + (((e - (k << log2G)) * B) >> 3), wd_[j]);
+        sd_[j] = ld_nc_f32(reinterpret_cast<const float *>(rec));
+      } else {
+        load_codes16<B>(codes + e * B / 8, wd_[j]);
+        sd_[j] = ld_nc_f32(scales + (e >> log2G));
+      }
     }
   };
 #pragma unroll
@@ -334,8 +384,16 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t *__r
     }
   }
   if (c.owns_tail(n)) {
-    for (int64_t i = nfull * kTile + c.lane; i < n; i += 32)
-      store1<DT>(dst, i, dequant1<FMT>(codes, i, scales[i >> log2G]));
+    for (int64_t i = nfull * kTile + c.lane; i < n; i += 32) {
+      if constexpr (IL) {
+        const int64_t k = i >> log2G;
+        const uint8_t *rec = codes + k * il_stride<B>(log2G);
+        store1<DT>(dst, i, dequant1<FMT>(rec + 4, i - (k << log2G),
+                                         *reinterpret_cast<const float *>(rec)));
+      } else {
+        store1<DT>(dst, i, dequant1<FMT>(codes, i, scales[i >> log2G]));
+      }
+    }
   }
 }
 

@@ -207,7 +207,8 @@ zq_status zq_quantize_reordered(const void *src, int src_dtype, int64_t n, int f
  *     those fp32 sums. out[g] is the reduced chunk g.
  * Each sum is exactly zq_reduce_quantized's (+0.0f, then one binary32 add per
  * term in the order given); the hop-1 results pass through format_mid, as the
- * pages' protocol sends them. 2 * P reduce launches are enqueued on `stream`.
+ * pages' protocol sends them. Two reduce launches (one per hop, each over all
+ * P GPUs' problems) are enqueued on `stream`.
  *   all pointer arrays   HOST arrays of P device pointers; mid_codes[g] holds
  *                        zq_codes_bytes(format_mid, nodes * m) bytes and
  *                        mid_scales[g] zq_num_blocks(nodes * m, G_mid) floats;
@@ -221,6 +222,61 @@ zq_status zq_reduce_two_hop(const void *const *codes, const float *const *scales
                             void *const *mid_codes, float *const *mid_scales, int format_mid,
                             int64_t G_mid, void *const *out_codes, float *const *out_scales,
                             int format_out, int64_t G_out, float *const *sums, void *stream);
+
+/*
+ * zq_interleaved_bytes -- bytes of the metadata-interleaved record stream of
+ * n elements ([Aquavit] summary of the implementation, "metadata
+ * interleaving", and Eq. 6): one record per G-element block, the block's
+ * fp32 scale (4 bytes, little endian) followed by its packed codes (the
+ * LSB-first b-bit stream of zq_quantize restricted to the block: G*b/8
+ * bytes, or the code bits of a partial last block padded to whole 32-bit
+ * words). No padding between records, so the stream has exactly
+ * zq_codes_bytes(format, n) + 4 * zq_num_blocks(n, G) bytes and the width
+ * stays b + 32/G bits per element. Integer formats only: returns 0 for
+ * ZQ_E4M3, an unknown format or an invalid G.
+ */
+size_t zq_interleaved_bytes(int format, int64_t n, int64_t G);
+
+/*
+ * zq_quantize_interleaved -- zq_quantize writing the interleaved record
+ * stream instead of separate codes and scales. The codes and scales are
+ * exactly zq_quantize's, regrouped.
+ *   records  device, zq_interleaved_bytes(format, n, G) bytes, 16-byte aligned,
+ *            must not overlap src
+ *   format   ZQ_INT2, ZQ_INT4, ZQ_INT6 or ZQ_INT8 (ZQ_E4M3: ZQ_ERR_UNSUPPORTED)
+ * Other arguments and errors as zq_quantize.
+ */
+zq_status zq_quantize_interleaved(const void *src, int src_dtype, int64_t n, int format, int64_t G,
+                                  void *records, void *stream);
+
+/*
+ * zq_dequantize_interleaved -- zq_dequantize reading an interleaved record
+ * stream: y = fl32(q * s) with s the record's scale, then one RNE rounding to
+ * dst_dtype. Same results as zq_dequantize of the planar form.
+ *   records  device, zq_interleaved_bytes(format, n, G) bytes, 16-byte aligned
+ *   dst      device, n elements of dst_dtype; must not overlap records
+ * Other arguments and errors as zq_dequantize (integer formats only).
+ */
+zq_status zq_dequantize_interleaved(const void *records, int64_t n, int format, int64_t G,
+                                    void *dst, int dst_dtype, void *stream);
+
+/*
+ * zq_aquavit_schedule -- [Aquavit]'s ascending width schedule (summary and
+ * Section 5.1): the target width at step t of T is
+ *   bpw(t) = 8 - 6 / (a + c * t / T)       ((a, c) = (0.9, 5) on the pages),
+ * and the step uses the available pair (b in {2, 4, 6}, G in {32, ..., 1024};
+ * the pages' range 2.03 to 7.00 bits per element) whose b + 32/G is nearest
+ * to bpw(t), ties to the narrower pair. (The pages give no rule from width to
+ * pair; this nearest-width reading is the library's.) Host-only arithmetic.
+ *   t, T          0 <= t <= T, T >= 1
+ *   a, c          a > 0, c >= 0
+ *   format, G     out: ZQ_INT2 / ZQ_INT4 / ZQ_INT6 and the block size
+ *   target, width out (either may be NULL): bpw(t) and b + 32/G of the pair
+ * Returns ZQ_ERR_INVALID_ARG for arguments outside these ranges or NULL
+ * format / G.
+ */
+zq_status zq_aquavit_schedule(int64_t t, int64_t T, double a, double c, int *format, int64_t *G,
+                              double *target, double *width);
 
 /*
  * zq_fp8_accumulate -- in-place FP8 gradient accumulation ([AGoQ] 2.B "Local

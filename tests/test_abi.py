@@ -144,3 +144,55 @@ def test_fp8_accumulate_argument_errors(L):
     assert L.zq_fp8_accumulate(c, s, c + 1024, zq.BF16, 4096, 128, None) == ALIAS
     assert L.zq_fp8_accumulate(c, c + 2048, g, zq.BF16, 4096, 128, None) == ALIAS
     assert L.zq_fp8_accumulate(c, s, g, zq.BF16, 0, 128, None) == OK
+
+
+def test_interleaved_size_matches_the_oracle(L):
+    for fmt in (zq.INT2, zq.INT4, zq.INT6, zq.INT8):
+        for G in zq.BLOCK_SIZES:
+            for n in (0, 1, G - 1, G, G + 1, 3 * G, 67108864 + 5):
+                assert zq.interleaved_bytes(fmt, n, G) == O.il_bytes(fmt, n, G), (fmt, G, n)
+    assert zq.interleaved_bytes(zq.E4M3, 4096, 128) == 0 and O.il_bytes(O.E4M3, 4096, 128) == -1
+    assert zq.interleaved_bytes(zq.INT4, 4096, 48) == 0 and zq.interleaved_bytes(zq.INT4, -1, 32) == 0
+
+
+def test_interleaved_argument_errors(L):
+    src, rec, dst = BASE, BASE + (1 << 24), BASE + (1 << 26)
+    qi = lambda **k: L.zq_quantize_interleaved(k.get("src", src), k.get("dt", zq.BF16),  # noqa: E731
+                                               k.get("n", 4096), k.get("fmt", zq.INT4),
+                                               k.get("G", 128), k.get("rec", rec), None)
+    assert qi(fmt=zq.E4M3) == UNSUPPORTED and qi(fmt=3) == UNSUPPORTED and qi(dt=7) == UNSUPPORTED
+    assert qi(n=-1) == INVALID and qi(G=48) == INVALID
+    assert qi(n=0, src=None, rec=None) == OK
+    assert qi(src=None) == INVALID and qi(rec=None) == INVALID
+    assert qi(src=src + 8) == MISALIGNED and qi(rec=rec + 4) == MISALIGNED
+    assert qi(rec=src + 4096) == ALIAS  # records inside the 8 KiB source
+    di = lambda **k: L.zq_dequantize_interleaved(k.get("rec", rec), k.get("n", 4096),  # noqa: E731
+                                                 k.get("fmt", zq.INT4), k.get("G", 128),
+                                                 k.get("dst", dst), k.get("dt", zq.BF16), None)
+    assert di(fmt=zq.E4M3) == UNSUPPORTED and di(dt=9) == UNSUPPORTED
+    assert di(n=-5) == INVALID and di(G=100) == INVALID and di(rec=None) == INVALID
+    assert di(dst=dst + 8) == MISALIGNED and di(dst=rec + 1024) == ALIAS
+    assert di(n=0) == OK
+
+
+def test_aquavit_schedule_matches_the_oracle(L):
+    """Host-only arithmetic: the library's schedule and pair choice against the
+    oracle's for the pages' default and two other settings, every step."""
+    for a, c, T in ((0.9, 5.0, 1000), (0.5, 2.0, 300), (2.0, 9.0, 77)):
+        for t in range(T + 1):
+            fmt, G, want, width = zq.aquavit_schedule(t, T, a, c)
+            b, oG, ow = O.aquavit_pick(O.aquavit_bpw(t, T, a, c))
+            assert (fmt, G, width) == (b, oG, ow), (a, c, T, t)
+            assert want == O.aquavit_bpw(t, T, a, c)
+
+
+def test_aquavit_schedule_argument_errors(L):
+    f, G = ctypes.c_int(0), ctypes.c_int64(0)
+    s = lambda t, T, a=0.9, c=5.0, fp=ctypes.byref(f), gp=ctypes.byref(G): \
+        L.zq_aquavit_schedule(t, T, a, c, fp, gp, None, None)  # noqa: E731
+    assert s(0, 1000) == OK and (f.value, G.value) == (zq.INT2, 1024)
+    assert s(1000, 1000) == OK and (f.value, G.value) == (zq.INT6, 32)
+    assert s(-1, 10) == INVALID and s(11, 10) == INVALID and s(0, 0) == INVALID
+    assert s(0, 10, a=0.0) == INVALID and s(0, 10, c=-1.0) == INVALID
+    assert s(0, 10, a=float("nan")) == INVALID and s(0, 10, c=float("inf")) == INVALID
+    assert s(0, 10, fp=None) == INVALID and s(0, 10, gp=None) == INVALID
