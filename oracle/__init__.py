@@ -79,6 +79,8 @@ def _declare(lib):
     lib.orc_aquavit_bpw.restype = ctypes.c_double
     lib.orc_aquavit_pick.argtypes = [ctypes.c_double, ctypes.POINTER(i32), ctypes.POINTER(i64)]
     lib.orc_aquavit_pick.restype = ctypes.c_double
+    lib.orc_reduce_ring.argtypes = [vp, vp, i32, i64, i32, i64, vp, vp, vp, vp, i32, i64, vp]
+    lib.orc_reduce_ring.restype = i32
     lib.orc_encode_n.argtypes = [i32, vp, i64, vp]
     lib.orc_decode_n.argtypes = [i32, vp, i64, vp]
     lib.orc_encode_n.restype = i32
@@ -221,6 +223,30 @@ def aquavit_pick(bpw: float, lib=None):
     b, G = ctypes.c_int(0), ctypes.c_int64(0)
     w = lib.orc_aquavit_pick(bpw, ctypes.byref(b), ctypes.byref(G))
     return b.value, G.value, float(w)
+
+
+def reduce_ring(codes_list, scales_list, n: int, fmt: int, G: int, fmt_out: int, G_out: int,
+                want_sum: bool = False, lib=None):
+    """The ring reduce-scatter's hops for one chunk: (codes, scales, sum_or_None)."""
+    lib = lib or load()
+    codes_list = [np.ascontiguousarray(c, dtype=np.uint8) for c in codes_list]
+    scales_list = [np.ascontiguousarray(s, dtype=np.float32) for s in scales_list]
+    N = len(codes_list)
+    cp = (ctypes.c_void_p * N)(*[_ptr(c) for c in codes_list])
+    sp = (ctypes.c_void_p * N)(*[_ptr(s) for s in scales_list])
+    part_c = [np.zeros(codes_bytes(fmt, n, lib), np.uint8) for _ in range(2)]
+    part_s = [np.zeros(max(num_blocks(n, G, lib), 1), np.float32) for _ in range(2)]
+    pcp = (ctypes.c_void_p * 2)(*[_ptr(c) for c in part_c])
+    psp = (ctypes.c_void_p * 2)(*[_ptr(s) for s in part_s])
+    out_codes = np.full(codes_bytes(fmt_out, n, lib), GARBAGE, dtype=np.uint8)
+    out_scales = np.full(max(num_blocks(n, G_out, lib), 0), np.nan, dtype=np.float32)
+    sum_out = np.full(n, np.nan, dtype=np.float32) if want_sum else None
+    rc = lib.orc_reduce_ring(ctypes.addressof(cp), ctypes.addressof(sp), N, n, fmt, G,
+                             ctypes.addressof(pcp), ctypes.addressof(psp), _ptr(out_codes),
+                             _ptr(out_scales), fmt_out, G_out, _ptr(sum_out) if want_sum else None)
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out_codes, out_scales, sum_out
 
 
 def slice_position(c: int, A: int, L: int) -> int:

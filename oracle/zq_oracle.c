@@ -83,6 +83,14 @@
  *      {32,...,1024} whose b + 32/G is nearest to bpw(t), ties to the
  *      narrower. (The pages' mean of 5.79 bits over 1000 steps is not met by
  *      this or by the continuous schedule, whose mean is 5.74.)
+ *  R15 the ring reduce-scatter that qgZ replaces ([ZeRO++] "QGZ keeps
+ *      reductions in full precision while sending quantized gradients":
+ *      every hop dequantizes, adds and requantizes): the partial sum of a
+ *      chunk travels in the gradients' own format (b, G); hop r (r = 1 ..
+ *      N-1) computes acc = fl(D(partial) + D(shard r)) -- the reduce of R7
+ *      over the two terms [partial, shard r] -- and requantizes it; the
+ *      first partial is shard 0 itself; the last hop keeps acc (the fp32
+ *      result) and requantizes it to the output format.
  */
 #include <math.h>
 #include <stddef.h>
@@ -630,4 +638,40 @@ double orc_aquavit_pick(double bpw, int *bits, int64_t *G)
             }
         }
     return best;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Ring reduce-scatter hops (reading R15), for the accuracy comparison      */
+/* ------------------------------------------------------------------------ */
+
+/* Reduce N shards (fmt, G) the ring way: partial_0 = shard 0; for r = 1 ..
+ * N-1, acc = fl(D(partial_{r-1}) + D(shard r)); partial_r = quantize(acc)
+ * with (fmt, G) for r < N-1 and with (fmt_out, G_out) into out for r = N-1,
+ * whose acc goes to sum_out (optional). One shard: out = quantize(D(shard 0)).
+ * pc[0..1], ps[0..1]: two partial buffers of n elements in (fmt, G). */
+int orc_reduce_ring(const uint8_t *const *codes, const float *const *scales, int nshards, int64_t n,
+                    int fmt, int64_t G, uint8_t *const *pc, float *const *ps, uint8_t *out_codes,
+                    float *out_scales, int fmt_out, int64_t G_out, float *sum_out)
+{
+    const uint8_t *sc[2];
+    const float *ss[2];
+    int r, rc;
+    if (nshards < 1 || nshards > 64) return ORC_BAD;
+    if (nshards == 1)
+        return orc_reduce(codes, scales, 1, n, fmt, G, out_codes, out_scales, fmt_out, G_out, sum_out);
+    sc[0] = codes[0];
+    ss[0] = scales[0];
+    for (r = 1; r < nshards; ++r) {
+        sc[1] = codes[r];
+        ss[1] = scales[r];
+        if (r < nshards - 1) {
+            rc = orc_reduce(sc, ss, 2, n, fmt, G, pc[r % 2], ps[r % 2], fmt, G, 0);
+            sc[0] = pc[r % 2];
+            ss[0] = ps[r % 2];
+        } else {
+            rc = orc_reduce(sc, ss, 2, n, fmt, G, out_codes, out_scales, fmt_out, G_out, sum_out);
+        }
+        if (rc != ORC_OK) return rc;
+    }
+    return ORC_OK;
 }

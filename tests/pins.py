@@ -791,6 +791,77 @@ def pin_schedule_pick(lib):
         prev = w
 
 
+# ---------------------------------------------------------------------------
+# The ring reduce-scatter that qgZ replaces ([ZeRO++] "QGZ keeps reductions in
+# full precision while sending quantized gradients"; reading R15).
+# ---------------------------------------------------------------------------
+
+def pin_ring_small_n(lib):
+    """One or two shards: the ring has no intermediate requantization, so it is
+    the one-hop reduce exactly."""
+    r = rng(41)
+    n = 3000
+    for N in (1, 2):
+        xs = [(r.laplace(0, 1e-3, n)).astype(np.float32) for _ in range(N)]
+        q = [O.quantize(x, O.INT4, 128, lib=lib) for x in xs]
+        a = O.reduce_ring([c for c, _ in q], [sc for _, sc in q], n, O.INT4, 128, O.INT8, 64,
+                          want_sum=True, lib=lib)
+        b = O.reduce([c for c, _ in q], [sc for _, sc in q], n, O.INT4, 128, O.INT8, 64,
+                     want_sum=True, lib=lib)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(as_u32(a[1]), as_u32(b[1]))
+        assert np.array_equal(as_u32(a[2]), as_u32(b[2])), N
+
+
+def as_u32(a):
+    return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+
+
+def pin_ring_exact_sums(lib):
+    """int8, G = 32, values q * 2^-9: in every block shard s holds +-127 at
+    element s, where the other shards hold 0, and small integers elsewhere,
+    so that no prefix sum leaves [-127, 127]. Every shard and every partial
+    sum then has block absmax 127 * 2^-9, i.e. scale exactly 2^-9, every
+    (re)quantization is exact, and the ring's fp32 result equals the integer
+    sum."""
+    k, N, nb = -9, 6, 64
+    for G in (32, 128):
+        r = np.random.default_rng([9, G])
+        ints = []
+        for s in range(N):
+            q = r.integers(-127 // N, 127 // N + 1, nb * G)
+            for s2 in range(N):
+                q[s2::G] = 0
+            q[s::G] = 127 * np.where(r.random(nb) < 0.5, 1, -1)
+            ints.append(q.astype(np.int64))
+        xs = [(q * 2.0 ** k).astype(np.float32) for q in ints]
+        qs = [O.quantize(x, O.INT8, G, lib=lib) for x in xs]
+        _, _, sm = O.reduce_ring([c for c, _ in qs], [sc for _, sc in qs], nb * G, O.INT8, G, O.INT8,
+                                 G, want_sum=True, lib=lib)
+        assert np.array_equal(sm, (np.sum(ints, axis=0) * 2.0 ** k).astype(np.float32)), G
+
+
+def pin_ring_requantizes_partials(lib):
+    """Three int8 shards of one block: 127 at element 0 of shard 0, 2^-7 at
+    element 1 of shard 1, zeros in shard 2. The ring requantizes 127 + 2^-7
+    with scale 1, which rounds the small term away (result 127 and 0); the
+    one-hop reduce keeps it; a ring run in the reverse order keeps it too."""
+    G, n = 32, 32
+    x0 = np.zeros(n, np.float32); x0[0] = 127.0
+    x1 = np.zeros(n, np.float32); x1[1] = 2.0 ** -7
+    x2 = np.zeros(n, np.float32)
+    q = [O.quantize(x, O.INT8, G, lib=lib) for x in (x0, x1, x2)]
+    _, _, ring = O.reduce_ring([c for c, _ in q], [sc for _, sc in q], n, O.INT8, G, O.INT8, G,
+                               want_sum=True, lib=lib)
+    _, _, one = O.reduce([c for c, _ in q], [sc for _, sc in q], n, O.INT8, G, O.INT8, G,
+                         want_sum=True, lib=lib)
+    assert ring[0] == 127.0 and ring[1] == 0.0 and np.all(ring[2:] == 0.0)
+    assert one[0] == 127.0 and abs(float(one[1]) - 2.0 ** -7) < 2.0 ** -20
+    q.reverse()
+    _, _, rev = O.reduce_ring([c for c, _ in q], [sc for _, sc in q], n, O.INT8, G, O.INT8, G,
+                              want_sum=True, lib=lib)
+    assert rev[1] != 0.0
+
+
 FAST_PINS = [
     pin_bpw_endpoints, pin_bpw_formula, pin_zeropp_payload, pin_bit_layout,
     pin_e4m3_points, pin_e4m3_vs_library, pin_f16_vs_library, pin_bf16_vs_library,
@@ -801,5 +872,6 @@ FAST_PINS = [
     pin_fp8_reduce_no_overflow, pin_fp8_accumulate, pin_fp8_accumulate_two_roundings,
     pin_reordered_quantize_identity, pin_two_hop_ownership, pin_two_hop_exact_sums,
     pin_two_hop_order, pin_il_size, pin_il_hand_records, pin_il_is_a_regrouping,
-    pin_schedule_closed_forms, pin_schedule_pick,
+    pin_schedule_closed_forms, pin_schedule_pick, pin_ring_small_n, pin_ring_exact_sums,
+    pin_ring_requantizes_partials,
 ]

@@ -101,6 +101,19 @@ MUTANTS = [
     ("pick_rounds_up", "double w = b + 32.0 / (double)g, d = fabs(w - bpw);",
      "double w = b + 32.0 / (double)g, d = (w >= bpw) ? w - bpw : 1e9;"),
     ("pick_allows_8_bit", "for (b = 2; b <= 6; b += 2)", "for (b = 2; b <= 8; b += 2)"),
+    ("ring_is_one_hop", "    if (nshards == 1)\n        return orc_reduce(codes, scales, 1, n,",
+     "    if (nshards >= 1)\n        return orc_reduce(codes, scales, nshards, n,"),
+    ("ring_reverse_chain",
+     "    sc[0] = codes[0];\n    ss[0] = scales[0];\n    for (r = 1; r < nshards; ++r) {\n"
+     "        sc[1] = codes[r];\n        ss[1] = scales[r];",
+     "    sc[0] = codes[nshards - 1];\n    ss[0] = scales[nshards - 1];\n    for (r = 1; r < nshards; ++r) {\n"
+     "        sc[1] = codes[nshards - 1 - r];\n        ss[1] = scales[nshards - 1 - r];"),
+    # (same sizes: int8 partials written as E4M3 bytes and read back as int8)
+    ("ring_partial_in_another_format",
+     "rc = orc_reduce(sc, ss, 2, n, fmt, G, pc[r % 2], ps[r % 2], fmt, G, 0);",
+     "rc = orc_reduce(sc, ss, 2, n, fmt, G, pc[r % 2], ps[r % 2], fmt == ORC_INT8 ? ORC_E4M3 : fmt, G, 0);"),
+    ("ring_skips_last_hop", "    for (r = 1; r < nshards; ++r) {\n        sc[1] = codes[r];",
+     "    for (r = 1; r < nshards - 1; ++r) {\n        sc[1] = codes[r];"),
 ]
 
 
