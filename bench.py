@@ -520,6 +520,121 @@ class QgzReduce:
                              "single thread")
 
 
+class RingStudy(QgzReduce):
+    """The ring reduce-scatter that qgZ replaces, against qgZ's one-hop
+    reduce, on the qgz_reduce shards (8 x 134,217,728 int4 G=128 from
+    Laplace(0, 1e-4) gradients): one-hop = one launch that dequantizes all 8
+    shards, sums in fp32 and requantizes once; ring = 7 sequential hops, each
+    a dequantize-add-requantize of [partial, next shard] with the partial in
+    int4 G=128. Both keep the fp32 sums. After the timed steps the fp32
+    results are compared with the exact (float64) sum of the unquantized
+    gradients on the first 16,777,216 elements."""
+
+    name = "ring_study"
+    dtype = "int4 codes + fp32 scales in, fp32 sums, int4 codes out (fp32 arithmetic)"
+
+    def config(self):
+        c = {"workload": "ring_study: 8 simulated peer shards of 134,217,728 fp32 gradients "
+                         "~Laplace(0,1e-4), pre-quantized to int4 G=128; qgZ one-hop reduce "
+                         "(dequant all, fp32 sum, requant once) vs ring reduce-scatter (7 "
+                         "sequential dequant-add-requant hops, partials in int4 G=128); fp32 sums "
+                         "kept by both",
+             "elements": self.n, "shards": self.N,
+             "l2": "no flush: 570 MB of shard input per one-hop launch; each ring hop reads "
+                   "142 MB and writes 71 MB (>> 126 MB L2 across hops)"}
+        if hasattr(self, "sum_one"):
+            c["accuracy"] = self.accuracy()
+        return c
+
+    def setup(self):
+        super().setup()
+        zq, n = self.zq, self.n
+        import torch
+
+        self.sum_one = torch.empty(n, dtype=torch.float32, device="cuda")
+        self.sum_ring = torch.empty(n, dtype=torch.float32, device="cuda")
+        self.ocr, self.osr = zq.empty_codes(zq.INT4, n, "cuda"), zq.empty_scales(n, 128, "cuda")
+        self.partials = [(zq.empty_codes(zq.INT4, n, "cuda"), zq.empty_scales(n, 128, "cuda"))
+                         for _ in range(2)]
+
+    def _one(self):
+        zq = self.zq
+        zq.reduce_quantized(self.codes, self.scales, self.n, zq.INT4, 128, zq.INT4, 128, self.oc4,
+                            self.os4, sum_out=self.sum_one)
+
+    def _ring(self):
+        zq = self.zq
+        zq.reduce_ring(self.codes, self.scales, self.n, zq.INT4, 128, zq.INT4, 128, self.ocr,
+                       self.osr, sum_out=self.sum_ring, partials=self.partials)
+
+    def launches(self):
+        n, N = self.n, self.N
+        p4 = packed_bytes(4, n, 128)
+        return [Launch("one-hop reduce 8x int4 G=128 -> int4 G=128 + fp32 sums", "reduce one-hop",
+                       N * p4 + p4 + 4 * n, self._one),
+                Launch("ring 7 hops of 2x int4 G=128 -> int4 G=128 (+ fp32 sums at the end)",
+                       "reduce ring hop", (N - 1) * 3 * p4 + 4 * n, self._ring, kernels=N - 1)]
+
+    def accuracy(self, m=1 << 24):
+        import torch
+
+        torch.cuda.synchronize()
+        exact = np.zeros(m, np.float64)
+        for x in self.host_sample:
+            exact += x[:m].astype(np.float64)
+        ref = float(np.sqrt(np.mean(exact ** 2)))
+        out = {"elements": m, "reference": "float64 sum of the unquantized fp32 gradients"}
+        for key, t in (("one_hop", self.sum_one), ("ring", self.sum_ring)):
+            e = t[:m].cpu().numpy().astype(np.float64) - exact
+            out[key] = {"rel_rms_error": round(float(np.sqrt(np.mean(e ** 2))) / ref, 5),
+                        "max_abs_error": float(np.max(np.abs(e)))}
+        return out
+
+    def setup_e2e(self):
+        import torch
+
+        zq, n = self.zq, self.n
+        self.h_codes = [c.cpu().pin_memory() for c in self.codes]
+        self.h_scales = [s.cpu().pin_memory() for s in self.scales]
+        self.h_oc = torch.empty(zq.codes_bytes(zq.INT4, n), dtype=torch.uint8).pin_memory()
+        self.h_os = torch.empty(zq.num_blocks(n, 128), dtype=torch.float32).pin_memory()
+        inb = self.N * packed_bytes(4, n, 128)
+        return inb, 2 * packed_bytes(4, n, 128)
+
+    def e2e_step(self):
+        """Shards from host memory once; both schemes; both results to host memory."""
+        for r in range(self.N):
+            self.codes[r].copy_(self.h_codes[r], non_blocking=True)
+            self.scales[r].copy_(self.h_scales[r], non_blocking=True)
+        for run, oc, os_ in ((self._one, self.oc4, self.os4), (self._ring, self.ocr, self.osr)):
+            run()
+            self.h_oc.copy_(oc, non_blocking=True)
+            self.h_os.copy_(os_, non_blocking=True)
+
+    def e2e_bytes(self):
+        return sum(l.nbytes for l in self.launches())
+
+    def oracle_sample(self, sample=1 << 24):
+        import oracle as O
+        from blockwise_quantized_zero_gb300 import inputs
+
+        host = getattr(self, "host_sample", None)
+        if host is None or host[0].size < sample:
+            host = [inputs.gradient_shard_f32(sample, shard=r) for r in range(self.N)]
+        sh = [O.quantize(np.ascontiguousarray(x[:sample]), O.INT4, 128) for x in host]
+
+        def run():
+            O.reduce([c for c, _ in sh], [s for _, s in sh], sample, O.INT4, 128, O.INT4, 128,
+                     want_sum=True)
+            O.reduce_ring([c for c, _ in sh], [s for _, s in sh], sample, O.INT4, 128, O.INT4, 128,
+                          want_sum=True)
+
+        p4 = packed_bytes(4, sample, 128)
+        nbytes = self.N * p4 + p4 + 4 * sample + (self.N - 1) * 3 * p4 + 4 * sample
+        return run, nbytes, (f"first {sample:,} elements of each of the 8 shards, one-hop and ring, "
+                             "single thread")
+
+
 class QgzTwoHop:
     """qgZ's hierarchy simulated on one GPU: 2 nodes x 4 GPUs, each holding a
     134,217,728-element fp32 gradient ~ Laplace(0, 1e-4) (seed 3, stream = GPU,
@@ -1025,7 +1140,7 @@ class AquavitSchedule:
 
 WORKLOADS = {"gm_sweep": GMSweep, "qwz_fp16": QwzFP16, "qgz_reduce": QgzReduce,
              "agoq_fp8": AgoqFP8, "llama70b": Llama70B, "qgz_two_hop": QgzTwoHop,
-             "aquavit_schedule": AquavitSchedule}
+             "aquavit_schedule": AquavitSchedule, "ring_study": RingStudy}
 
 
 # ---------------------------------------------------------------------------

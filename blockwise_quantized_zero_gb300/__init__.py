@@ -71,6 +71,8 @@ def _declare(L):
                                       ctypes.POINTER(i32), ctypes.POINTER(i64),
                                       ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
     L.zq_aquavit_schedule.restype = i32
+    L.zq_reduce_ring.argtypes = [vp, vp, i32, i64, i32, i64, vp, vp, vp, vp, i32, i64, vp, vp]
+    L.zq_reduce_ring.restype = i32
     L.zq_status_string.argtypes = [i32]
     L.zq_status_string.restype = ctypes.c_char_p
     L.zq_last_cuda_error.argtypes = []
@@ -176,6 +178,33 @@ def dequantize(codes, scales, n: int, fmt: int, G: int, out_dtype=None, out=None
     _check(lib().zq_dequantize(codes.data_ptr(), scales.data_ptr(), n, fmt, G, out.data_ptr(),
                                dtype_code(out.dtype), _stream(codes, stream)), "zq_dequantize")
     return out
+
+
+def reduce_ring(codes_list, scales_list, n: int, fmt: int, G: int, fmt_out: int, G_out: int,
+                out_codes=None, out_scales=None, sum_out=None, partials=None, stream=None):
+    """The ring reduce-scatter's hops (dequantize, add, requantize per hop) for
+    one chunk -> (codes, scales, sum or None). partials: two (codes, scales)
+    buffer pairs in (fmt, G), allocated here when not given."""
+    torch = _torch()
+    N = len(codes_list)
+    if N != len(scales_list):
+        raise ValueError("codes_list and scales_list differ in length")
+    dev = codes_list[0].device
+    out_codes = empty_codes(fmt_out, n, dev) if out_codes is None else out_codes
+    out_scales = empty_scales(n, G_out, dev) if out_scales is None else out_scales
+    if sum_out is True:
+        sum_out = torch.empty(n, dtype=torch.float32, device=dev)
+    if partials is None and N >= 3:
+        partials = [(empty_codes(fmt, n, dev), empty_scales(n, G, dev)) for _ in range(2)]
+    cp = (ctypes.c_void_p * N)(*[c.data_ptr() for c in codes_list])
+    sp = (ctypes.c_void_p * N)(*[s.data_ptr() for s in scales_list])
+    pc = (ctypes.c_void_p * 2)(*[c.data_ptr() for c, _ in partials]) if partials else None
+    ps = (ctypes.c_void_p * 2)(*[s.data_ptr() for _, s in partials]) if partials else None
+    _check(lib().zq_reduce_ring(cp, sp, N, n, fmt, G, pc, ps, out_codes.data_ptr(),
+                                out_scales.data_ptr(), fmt_out, G_out,
+                                sum_out.data_ptr() if sum_out is not None else None,
+                                _stream(out_codes, stream)), "zq_reduce_ring")
+    return out_codes, out_scales, sum_out
 
 
 def interleaved_bytes(fmt: int, n: int, G: int) -> int:

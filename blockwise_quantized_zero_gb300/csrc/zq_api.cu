@@ -461,6 +461,89 @@ zq_status zq_reduce_quantized(const void *const *codes, const float *const *scal
   return from_cuda(launch_reduce(a, format_in, format_out, as_stream(stream)));
 }
 
+zq_status zq_reduce_ring(const void *const *codes, const float *const *scales, int nshards,
+                         int64_t n, int format, int64_t G, void *const *partial_codes,
+                         float *const *partial_scales, void *out_codes, float *out_scales,
+                         int format_out, int64_t G_out, float *sum_out, void *stream) {
+  // partial buffers are used from three shards on; their argument checks come
+  // first, the device-pointer checks after the shared reduce checks
+  const bool chain = nshards > 2 && nshards <= ZQ_MAX_SHARDS && n > 0 && bits_of(format) &&
+                     bits_of(format_out) && valid_block(G) && valid_block(G_out);
+  if (chain) {
+    if (!codes || !scales || !out_codes || !out_scales) return ZQ_ERR_INVALID_ARG;
+    for (int r = 0; r < nshards; ++r)
+      if (!codes[r] || !scales[r]) return ZQ_ERR_INVALID_ARG;
+    if (!partial_codes || !partial_scales) return ZQ_ERR_INVALID_ARG;
+    std::vector<Range> held;  // every buffer the chain reads or writes
+    for (int r = 0; r < nshards; ++r) {
+      held.emplace_back(codes[r], zq_codes_bytes(format, n));
+      held.emplace_back(scales[r], size_t(zq_num_blocks(n, G)) * 4u);
+    }
+    held.emplace_back(out_codes, zq_codes_bytes(format_out, n));
+    held.emplace_back(out_scales, size_t(zq_num_blocks(n, G_out)) * 4u);
+    held.emplace_back(sum_out, sum_out ? size_t(n) * 4u : 0u);
+    for (int k = 0; k < 2; ++k) {
+      if (!partial_codes[k] || !partial_scales[k]) return ZQ_ERR_INVALID_ARG;
+      if (!aligned16(partial_codes[k]) || !aligned16(partial_scales[k])) return ZQ_ERR_MISALIGNED;
+      const Range pc(partial_codes[k], zq_codes_bytes(format, n)),
+          ps(partial_scales[k], size_t(zq_num_blocks(n, G)) * 4u);
+      for (const Range &h : held)
+        if (h.overlaps(pc) || h.overlaps(ps)) return ZQ_ERR_ALIAS;
+      if (pc.overlaps(ps)) return ZQ_ERR_ALIAS;
+      held.push_back(pc);
+      held.push_back(ps);
+    }
+  }
+  if (zq_status st = check_reduce(codes, scales, nshards, ZQ_MAX_SHARDS, n, format, G, out_codes,
+                                  out_scales, format_out, G_out, sum_out))
+    return st;
+  if (n == 0) return ZQ_OK;
+  if (chain)
+    for (int k = 0; k < 2; ++k) {
+      if (zq_status st = check_device_ptr(partial_codes[k])) return st;
+      if (zq_status st = check_device_ptr(partial_scales[k])) return st;
+    }
+  // hop r: the shard-ordered reduce of [partial, shard r], requantized into
+  // the ring format (partial buffer r % 2) or, at the last hop, the output
+  ReduceArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.n = n;
+  a.log2Gin = log2_block(G);
+  a.one = 1.0f;
+  if (nshards == 1) {
+    a.codes[0] = static_cast<const uint8_t *>(codes[0]);
+    a.scales[0] = scales[0];
+    a.nshards = 1;
+    a.out_codes = static_cast<uint8_t *>(out_codes);
+    a.out_scales = out_scales;
+    a.sum_out = sum_out;
+    a.log2Gout = log2_block(G_out);
+    a.wide = (!sum_out || aligned32(sum_out)) ? 1 : 0;
+    return from_cuda(launch_reduce(a, format, format_out, as_stream(stream)));
+  }
+  const uint8_t *pcodes = static_cast<const uint8_t *>(codes[0]);
+  const float *pscales = scales[0];
+  a.nshards = 2;
+  for (int r = 1; r < nshards; ++r) {
+    const bool last = r == nshards - 1;
+    a.codes[0] = pcodes;
+    a.scales[0] = pscales;
+    a.codes[1] = static_cast<const uint8_t *>(codes[r]);
+    a.scales[1] = scales[r];
+    a.out_codes = static_cast<uint8_t *>(last ? out_codes : partial_codes[r % 2]);
+    a.out_scales = last ? out_scales : partial_scales[r % 2];
+    a.sum_out = last ? sum_out : nullptr;
+    a.log2Gout = log2_block(last ? G_out : G);
+    a.wide = (!a.sum_out || aligned32(a.sum_out)) ? 1 : 0;
+    if (zq_status st = from_cuda(launch_reduce(a, format, last ? format_out : format,
+                                               as_stream(stream))))
+      return st;
+    pcodes = a.out_codes;
+    pscales = a.out_scales;
+  }
+  return ZQ_OK;
+}
+
 zq_status zq_reduce_quantized_static(const void *const *codes, const float *const *scales,
                                      int nshards, int64_t n, int format_in, int64_t G_in,
                                      void *out_codes, float *out_scales, int format_out,

@@ -224,6 +224,30 @@ zq_status zq_reduce_two_hop(const void *const *codes, const float *const *scales
                             int format_out, int64_t G_out, float *const *sums, void *stream);
 
 /*
+ * zq_reduce_ring -- the ring reduce-scatter's sequential hops for one chunk,
+ * the scheme qgZ replaces ([ZeRO++] "QGZ keeps reductions in full precision
+ * while sending quantized gradients": in the ring, every hop dequantizes,
+ * adds and requantizes). Built for the accuracy comparison with
+ * zq_reduce_quantized (one requantization). With partial_0 = shard 0:
+ *   hop r = 1 .. nshards-1:  acc = fl32(D(partial_{r-1}) + D(shard r))
+ *     (zq_reduce_quantized over the two terms [partial, shard r]);
+ *     partial_r = requantize(format, G) of acc into partial buffer r % 2,
+ *     except at the last hop, which requantizes to (format_out, G_out) into
+ *     out and writes acc to sum_out (optional).
+ *   One shard: out = requantize(format_out, G_out) of D(shard 0).
+ * The partial sums travel in the shards' own format (format, G).
+ *   partial_codes, partial_scales  HOST arrays of 2 device pointers, each
+ *       zq_codes_bytes(format, n) bytes / zq_num_blocks(n, G) floats; used
+ *       (and required) only for nshards >= 3; no overlap with anything else
+ * Other arguments and errors as zq_reduce_quantized (format_in = format).
+ * nshards - 1 reduce launches (one for one shard) are enqueued on `stream`.
+ */
+zq_status zq_reduce_ring(const void *const *codes, const float *const *scales, int nshards,
+                         int64_t n, int format, int64_t G, void *const *partial_codes,
+                         float *const *partial_scales, void *out_codes, float *out_scales,
+                         int format_out, int64_t G_out, float *sum_out, void *stream);
+
+/*
  * zq_interleaved_bytes -- bytes of the metadata-interleaved record stream of
  * n elements ([Aquavit] summary of the implementation, "metadata
  * interleaving", and Eq. 6): one record per G-element block, the block's

@@ -196,3 +196,30 @@ def test_aquavit_schedule_argument_errors(L):
     assert s(0, 10, a=0.0) == INVALID and s(0, 10, c=-1.0) == INVALID
     assert s(0, 10, a=float("nan")) == INVALID and s(0, 10, c=float("inf")) == INVALID
     assert s(0, 10, fp=None) == INVALID and s(0, 10, gp=None) == INVALID
+
+
+def test_reduce_ring_argument_errors(L):
+    N, n = 4, 4096
+    cp = (ctypes.c_void_p * N)(*[BASE + i * (1 << 20) for i in range(N)])
+    sp = (ctypes.c_void_p * N)(*[BASE + (1 << 28) + i * (1 << 20) for i in range(N)])
+    oc, os_, sm = BASE + (1 << 30), BASE + (1 << 31), BASE + (1 << 32)
+    pc = (ctypes.c_void_p * 2)(BASE + (1 << 33), BASE + (1 << 33) + (1 << 20))
+    ps = (ctypes.c_void_p * 2)(BASE + (1 << 34), BASE + (1 << 34) + (1 << 20))
+
+    def r(**kw):
+        a = dict(N=N, n=n, fmt=zq.INT4, G=128, pc=pc, ps=ps, fout=zq.INT4, Gout=128, sm=sm)
+        a.update(kw)
+        return L.zq_reduce_ring(cp, sp, a["N"], a["n"], a["fmt"], a["G"], a["pc"], a["ps"], oc, os_,
+                                a["fout"], a["Gout"], a["sm"], None)
+
+    assert r(fmt=5) == UNSUPPORTED and r(N=0) == INVALID and r(N=65) == INVALID
+    assert r(G=48) == INVALID and r(n=-1) == INVALID and r(n=0) == OK
+    assert r(pc=None) == INVALID and r(ps=None) == INVALID  # three or more shards need partials
+    bad = (ctypes.c_void_p * 2)(BASE + (1 << 33) + 4, BASE + (1 << 33) + (1 << 20))
+    assert r(pc=bad) == MISALIGNED
+    onto_input = (ctypes.c_void_p * 2)(BASE + (1 << 20), BASE + (1 << 33) + (1 << 20))
+    assert r(pc=onto_input) == ALIAS
+    same = (ctypes.c_void_p * 2)(BASE + (1 << 33), BASE + (1 << 33))
+    assert r(pc=same) == ALIAS
+    onto_out = (ctypes.c_void_p * 2)(oc, BASE + (1 << 33) + (1 << 20))
+    assert r(pc=onto_out) == ALIAS
