@@ -999,18 +999,21 @@ class AquavitSchedule:
     name = "aquavit_schedule"
     dtype = "bf16 in, int2/4/6 codes + fp32 scales (interleaved records or planar), bf16 out"
     rows, cols = 8192, 8192
-    T, a, c = 1000, 0.9, 5.0
+    a, c = 0.9, 5.0
     slots = 8
 
-    def __init__(self):
+    def __init__(self, T=1000):
         from blockwise_quantized_zero_gb300 import inputs
 
+        if T < 1:
+            raise SystemExit("the schedule needs at least one step")
+        self.T = T
         self.n = self.rows * self.cols
         self.host = inputs.weight_shard_bf16(self.rows, self.cols)
 
     def config(self):
-        return {"workload": "aquavit_schedule: one 8192x8192 bf16 weight shard (N(0,0.02)); the "
-                            "1000-step ascending schedule bpw = 8 - 6/(0.9 + 5 t/1000), each step "
+        return {"workload": f"aquavit_schedule: one 8192x8192 bf16 weight shard (N(0,0.02)); the "
+                            f"{self.T}-step ascending schedule bpw = 8 - 6/(0.9 + 5 t/{self.T}), each step "
                             "quantize + dequantize->bf16 at its nearest (b, G); interleaved "
                             "records and planar layout, each for the whole schedule",
                 "elements": self.n, "schedule_steps": self.T, "a": self.a, "c": self.c,
@@ -1223,6 +1226,10 @@ def make_workload(args):
             raise SystemExit("--pair applies to --workload gm_sweep only")
         b, G = (int(v) for v in args.pair.split(":"))
         return GMSweep(pair=(b, G))
+    if args.schedule_steps is not None:
+        if args.workload != "aquavit_schedule":
+            raise SystemExit("--schedule-steps applies to --workload aquavit_schedule only")
+        return AquavitSchedule(T=args.schedule_steps)
     return WORKLOADS[args.workload]()
 
 
@@ -1445,6 +1452,9 @@ def main(argv=None):
     ap.add_argument("--oracle-sample", type=int, default=None,
                     help="elements in the CPU-oracle sample (default: the workload's own)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--schedule-steps", type=int, default=None,
+                    help="aquavit_schedule: schedule length T (default 1000, the pages' run); "
+                         "shorter schedules serve profiler captures")
     ap.add_argument("--pair", default=None,
                     help="gm_sweep only: run just one (b, G) pair, given as b:G (for profiling)")
     args = ap.parse_args(argv)
