@@ -34,10 +34,12 @@ template <auto Kernel, int SMEM = 0, int THREADS = kThreads> int ctas_per_sm() {
   return v;
 }
 
-// Persistent grid: enough CTAs for every warp tile, at most one wave.
-template <auto Kernel, int SMEM = 0> unsigned grid_for(int64_t n) {
+// Persistent grid: enough CTAs for every warp tile (or for every group of
+// tiles_per_warp tiles), at most one wave.
+template <auto Kernel, int SMEM = 0> unsigned grid_for(int64_t n, int tiles_per_warp = 1) {
   const int64_t tiles = (n + kTile - 1) / kTile;
-  const int64_t ctas = (tiles + kThreads / 32 - 1) / (kThreads / 32);
+  const int64_t per_cta = int64_t(kThreads / 32) * tiles_per_warp;
+  const int64_t ctas = (tiles + per_cta - 1) / per_cta;
   const int64_t cap = int64_t(device_sm_count()) * ctas_per_sm<Kernel, SMEM>();
   const int64_t g = ctas < cap ? ctas : cap;
   return static_cast<unsigned>(g > 0 ? g : 1);
@@ -69,6 +71,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, size_t smem, cud
                        Args... args) {
   return launch_pdl_threads(kernel, grid, kThreads, smem, st, args...);
 }
+
+// Quantize grids give every warp at least two tiles, so that the load of a
+// warp's next tile overlaps the current tile's arithmetic even for small
+// tensors (measured: 1 Mi-element calls, eight in flight, 4105 -> 4500 GB/s;
+// four tiles a warp left too few CTAs, 3178 GB/s). Large tensors are capped
+// at one wave either way.
+constexpr int kQuantizeTilesPerWarp = 2;
 
 // Launchers (one translation unit each). They return the launch status.
 cudaError_t launch_quantize(const void *src, int dt, int64_t n, int fmt, int64_t G, void *codes,

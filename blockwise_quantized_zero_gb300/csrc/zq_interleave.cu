@@ -9,7 +9,7 @@ namespace zq {
 template <int DT, int FMT, int G>
 static cudaError_t go_qi(const void *src, int64_t n, void *rec, cudaStream_t st, bool wide) {
   constexpr auto K = quantize_kernel<DT, FMT, G, true>;
-  return launch_pdl(K, grid_for<K>(n), 0, st, src, static_cast<uint8_t *>(rec),
+  return launch_pdl(K, grid_for<K>(n, kQuantizeTilesPerWarp), 0, st, src, static_cast<uint8_t *>(rec),
                     static_cast<float *>(nullptr), n, wide ? 1 : 0, SliceRemap{1, 1, 0});
 }
 

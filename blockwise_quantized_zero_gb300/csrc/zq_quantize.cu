@@ -8,7 +8,7 @@ template <int DT, int FMT, int G>
 static cudaError_t go_q(const void *src, int64_t n, void *codes, float *scales, cudaStream_t st,
                         bool wide, const SliceRemap &rm) {
   constexpr auto K = quantize_kernel<DT, FMT, G>;
-  return launch_pdl(K, grid_for<K>(n), 0, st, src, static_cast<uint8_t *>(codes), scales, n,
+  return launch_pdl(K, grid_for<K>(n, kQuantizeTilesPerWarp), 0, st, src, static_cast<uint8_t *>(codes), scales, n,
                     wide ? 1 : 0, rm);
 }
 
