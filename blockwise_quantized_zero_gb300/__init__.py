@@ -13,7 +13,15 @@ The operations (see ``include/zq.h`` for the exact definitions):
   * ``dequantize``        codes * scale, rounded to the output type;
   * ``reduce_quantized``  N quantized shards -> fp32 sum in shard order ->
                           requantized (ZeRO++ qgZ; AGoQ local reduce);
-  * ``fp8_accumulate``    in-place E4M3 main-gradient update (AGoQ QuanGrad).
+  * ``fp8_accumulate``    in-place E4M3 main-gradient update (AGoQ QuanGrad);
+  * ``quantize_reordered`` / ``reduce_two_hop``  qgZ's tensor-slice reordering
+                          fused into quantize, and its intra-node + inter-node
+                          reduce (ZeRO++ two-hop communication);
+  * ``reduce_ring``       the ring reduce-scatter's dequantize-add-requantize
+                          hops, for comparison with the one-hop reduce;
+  * ``quantize_interleaved`` / ``dequantize_interleaved``  Aquavit's metadata-
+                          interleaved block records (scale, then codes);
+  * ``aquavit_schedule``  Aquavit's ascending width schedule -> (b, G).
 """
 from __future__ import annotations
 
