@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libzq.so")
 
 UNITS = ["zq_api.cu", "zq_quantize.cu", "zq_dequantize.cu", "zq_reduce.cu", "zq_fp8.cu",
-         "zq_interleave.cu"]
+         "zq_interleave.cu", "zq_reduce_few.cu"]
 HEADERS = ["zq_device.cuh", "zq_kernels.cuh", "zq_host.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

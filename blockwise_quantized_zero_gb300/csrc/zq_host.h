@@ -97,8 +97,13 @@ cudaError_t launch_reduce_hop(const HopArgs &a, int fin, int fout, cudaStream_t 
 // arrays) are copied into a static device table on the stream.
 cudaError_t launch_reduce_static(const void *const *codes, const float *const *scales,
                                  const TableReduceArgs &args, int fin, int fout, cudaStream_t st);
+// The same two launches with the kernels built for three CTAs an SM (at most
+// kFewShards shards).
+cudaError_t launch_reduce_few(const ReduceArgs &a, int fin, int fout, cudaStream_t st);
+cudaError_t launch_reduce_hop_few(const HopArgs &a, int fin, int fout, cudaStream_t st);
 // Reads and clears the device error words of the launch units.
 unsigned take_reduce_device_error();
+unsigned take_reduce_few_device_error();
 
 cudaError_t launch_fp8_accumulate(void *codes, float *scales, const void *grad, int dt, int64_t n,
                                   int64_t G, cudaStream_t st, bool wide);

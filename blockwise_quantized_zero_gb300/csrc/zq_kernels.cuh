@@ -655,18 +655,27 @@ __device__ __forceinline__ void load_codes16_smem(const uint8_t *p, uint32_t (&w
 constexpr int kRedConsumers = 8;
 constexpr int kRedThreads = (kRedConsumers + 1) * 32;
 
-// Stage geometry (measured): 2-bit codes use four stages of up to 24 KB, wider
-// codes two stages of up to 40 KB (more shards per unit, fewer unit
-// overheads); two CTAs of 9 warps fit on an SM either way.
-template <int FIN> struct RedGeom {
+// Stage geometry, per the CTAs an SM holds (OCC, the kernel's launch bound;
+// measured on 134M int4 elements). OCC = 2 (up to 96 registers a thread):
+// 2-bit codes use four stages of up to 24 KB, wider codes two stages of up
+// to 40 KB (8 int4 shards a unit: more shards per unit, fewer unit
+// overheads). OCC = 3 (up to 72 registers), for launches of at most
+// kFewShards shards, where the requantization after every few shards is
+// latency-bound and more warps hide it: three stages of up to 24 KB (2
+// shards 168 -> 139 us, 4 shards 133 -> 129 us; 8 shards would lose, 194.5
+// -> 217 us).
+constexpr int kFewShards = 4;
+
+template <int FIN, int OCC = 2> struct RedGeom {
+  static_assert(OCC == 2 || OCC == 3, "reduce geometries exist for 2 and 3 CTAs an SM");
   static constexpr int kCodeBytes = kTile * Fmt<FIN>::kBits / 8;  // one shard, one tile
   static constexpr int kShardBytes =                               // codes + room for G_in = 32
       kRedConsumers * kCodeBytes + kRedConsumers * (kTile / 32) * 4;
-  static constexpr int kBudget = Fmt<FIN>::kBits <= 2 ? 24576 : 40960;
+  static constexpr int kBudget = (OCC == 3 || Fmt<FIN>::kBits <= 2) ? 24576 : 40960;
   static constexpr int kShards = (kBudget / kShardBytes) > 1 ? kBudget / kShardBytes : 1;
   static constexpr int kScaleOff = kShards * kRedConsumers * kCodeBytes;
   static constexpr int kStage = kShards * kShardBytes;
-  static constexpr int kStages = Fmt<FIN>::kBits <= 2 ? 4 : 2;
+  static constexpr int kStages = OCC == 3 ? 3 : (Fmt<FIN>::kBits <= 2 ? 4 : 2);
   static constexpr int kBarOff = kStages * kStage;
   static constexpr int kSmem = kBarOff + kStages * 16;  // full + empty barrier per stage
   static_assert(kCodeBytes % 16 == 0 && kStage % 16 == 0, "bulk copies need 16-byte multiples");
@@ -675,10 +684,10 @@ template <int FIN> struct RedGeom {
 // Device error word of this translation unit (read by zq_device_status).
 static __device__ unsigned int g_dev_error = 0;
 
-template <int FIN, int FOUT, typename A>
-__global__ void __launch_bounds__(kRedThreads, 2)
+template <int FIN, int FOUT, typename A, int OCC = 2>
+__global__ void __launch_bounds__(kRedThreads, OCC)
     reduce_kernel(const __grid_constant__ A a) {
-  using RG = RedGeom<FIN>;
+  using RG = RedGeom<FIN, OCC>;
   constexpr int BIN = Fmt<FIN>::kBits, WIN = Fmt<FIN>::kWords16, CB = RG::kCodeBytes;
   constexpr int S = RG::kStages;
   extern __shared__ __align__(128) uint8_t red_smem[];

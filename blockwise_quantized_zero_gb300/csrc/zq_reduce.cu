@@ -1,63 +1,23 @@
-// zq_reduce.cu -- launch unit for the quantized-reduce kernels (one
-// instantiation per input and output code format), and the reader of the
-// reduce kernels' device error word.
+// zq_reduce.cu -- launch unit for the quantized-reduce kernels built for two
+// CTAs an SM (one instantiation per input and output code format), the
+// allocation-free variant's shard table, and the reader of the reduce
+// kernels' device error words. Launches of at most kFewShards shards go to
+// the three-CTA instantiations of zq_reduce_few.cu.
 #include <cstddef>
 #include <mutex>
 
-#include "zq_host.h"
+#include "zq_reduce_launch.h"
 
 namespace zq {
 
-// Elements of all the problems of one launch.
-static int64_t launch_elements(const ReduceArgs &a) { return a.n; }
-static int64_t launch_elements(const TableReduceArgs &a) { return a.n; }
-static int64_t launch_elements(const HopArgs &a) {
-  return ((a.n + kTile * kRedConsumers - 1) / (kTile * kRedConsumers)) * kTile * kRedConsumers *
-         a.nprob;
-}
-
-// Persistent grid of CTAs of eight consumer warps and one producer warp: one
-// CTA per CTA tile (8192 elements), at most one wave.
-template <int FIN, int FOUT, typename A> static cudaError_t go_r(const A &a, cudaStream_t st) {
-  constexpr auto K = reduce_kernel<FIN, FOUT, A>;
-  constexpr int kSmem = RedGeom<FIN>::kSmem;
-  const int occ = ctas_per_sm<K, kSmem, kRedThreads>();
-  if (occ < 1) return cudaErrorInvalidConfiguration;
-  const int64_t span = int64_t(kRedConsumers) * kTile;
-  const int64_t ctas = (launch_elements(a) + span - 1) / span;
-  const int64_t cap = int64_t(device_sm_count()) * occ;
-  const unsigned grid = static_cast<unsigned>(ctas < 1 ? 1 : (ctas < cap ? ctas : cap));
-  return launch_pdl_threads(K, grid, kRedThreads, kSmem, st, a);
-}
-
-template <int FIN, typename A> static cudaError_t go_r_o(const A &a, int fout, cudaStream_t st) {
-  switch (fout) {
-    case F_INT2: return go_r<FIN, F_INT2>(a, st);
-    case F_INT4: return go_r<FIN, F_INT4>(a, st);
-    case F_INT6: return go_r<FIN, F_INT6>(a, st);
-    case F_INT8: return go_r<FIN, F_INT8>(a, st);
-    case F_E4M3: return go_r<FIN, F_E4M3>(a, st);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-template <typename A> static cudaError_t go_r_io(const A &a, int fin, int fout, cudaStream_t st) {
-  switch (fin) {
-    case F_INT2: return go_r_o<F_INT2>(a, fout, st);
-    case F_INT4: return go_r_o<F_INT4>(a, fout, st);
-    case F_INT6: return go_r_o<F_INT6>(a, fout, st);
-    case F_INT8: return go_r_o<F_INT8>(a, fout, st);
-    case F_E4M3: return go_r_o<F_E4M3>(a, fout, st);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
 cudaError_t launch_reduce(const ReduceArgs &a, int fin, int fout, cudaStream_t st) {
-  return go_r_io(a, fin, fout, st);
+  if (a.nshards <= kFewShards) return launch_reduce_few(a, fin, fout, st);
+  return go_r_io<2>(a, fin, fout, st);
 }
 
 cudaError_t launch_reduce_hop(const HopArgs &a, int fin, int fout, cudaStream_t st) {
-  return go_r_io(a, fin, fout, st);
+  if (a.nshards <= kFewShards) return launch_reduce_hop_few(a, fin, fout, st);
+  return go_r_io<2>(a, fin, fout, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -111,20 +71,11 @@ cudaError_t launch_reduce_static(const void *const *codes, const float *const *s
   if (e != cudaSuccess) return e;
   TableReduceArgs a = args;
   a.tab = tab;
-  return go_r_io(a, fin, fout, st);
+  return go_r_io<2>(a, fin, fout, st);
 }
 
 unsigned take_reduce_device_error() {
-  unsigned v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_dev_error, sizeof v) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return 0;
-  }
-  if (v != 0) {
-    const unsigned zero = 0;
-    (void)cudaMemcpyToSymbol(g_dev_error, &zero, sizeof zero);
-  }
-  return v;
+  return take_unit_error_word() | take_reduce_few_device_error();
 }
 
 }  // namespace zq
