@@ -109,3 +109,45 @@ def test_two_hop_argument_errors(zq):
     out = [(mid[g][0], mid[g][1]) for g in range(P)]  # outputs on top of the hop-1 buffers
     with pytest.raises(zq.ZQError, match="ALIAS"):
         zq.reduce_two_hop(c, s, A, L, n, O.INT4, 128, O.INT4, 128, O.INT4, 128, mid=mid, out=out)
+
+
+def test_two_hop_full_size_sampled(zq):
+    """The benchmark configuration (2 nodes x 4 GPUs, 134,217,728 fp32 per GPU,
+    int4 G=128 throughout), through the same calls the benchmark times. GPU
+    g's final chunk is the sum of chunk g of every gradient, so a window of
+    whole blocks of it follows from the same window of chunk g on every GPU:
+    the oracle quantizes those windows, sums them node by node (hop 1) and
+    over the nodes (hop 2), and must reproduce the GPU's codes, scales and
+    fp32 sums there."""
+    import torch
+
+    from blockwise_quantized_zero_gb300 import inputs
+
+    A, L, n, G = 2, 4, 134217728, 128
+    P, m = A * L, n // (A * L)
+    hx, qd = [], []
+    for g in range(P):
+        x = inputs.gradient_shard_f32(n, shard=g)
+        xd = torch.from_numpy(x).cuda()
+        qd.append(zq.quantize_reordered(xd, O.INT4, G, A, L))
+        del xd
+        hx.append(x)
+    _, out, sums = zq.reduce_two_hop([c for c, _ in qd], [s for _, s in qd], A, L, n, O.INT4, G,
+                                     O.INT4, G, O.INT4, G, sums=True)
+    zq.device_status()
+    W = 4096
+    rng = np.random.default_rng(17)
+    for g, lo in [(0, 0), (P - 1, m - W)] + [(int(rng.integers(0, P)), int(rng.integers(0, (m - W) // G)) * G)
+                                             for _ in range(4)]:
+        win = [O.quantize(np.ascontiguousarray(hx[g2][g * m + lo:g * m + lo + W]), O.INT4, G)
+               for g2 in range(P)]
+        mid = []
+        for a2 in range(A):  # hop 1: node a2's GPUs in order
+            part = [win[a2 * L + l2] for l2 in range(L)]
+            mc, ms, _ = O.reduce([c for c, _ in part], [s for _, s in part], W, O.INT4, G, O.INT4, G)
+            mid.append((mc, ms))
+        wc, ws, wsum = O.reduce([c for c, _ in mid], [s for _, s in mid], W, O.INT4, G, O.INT4, G,
+                                want_sum=True)
+        _same(to_host(sums[g][lo:lo + W]), wsum, f"GPU {g} sums at {lo}")
+        _same(to_host(out[g][1][lo // G:(lo + W) // G]), ws, f"GPU {g} scales at {lo}")
+        _same(to_host(out[g][0][lo // 2:(lo + W) // 2]), wc, f"GPU {g} codes at {lo}")
