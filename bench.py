@@ -8,7 +8,11 @@ bytes. Other workloads (``--workload``): qwz_fp16 (1 Mi fp16 weights with
 outliers, int8 G=256, batched over 512 tensors), qgz_reduce (8 int4 shards of
 134,217,728 gradients -> int4 G=128 and int8 G=256), agoq_fp8 (E4M3 main
 gradient of 268,435,456 elements, 4 accumulate steps + 8-shard FP8 reduce),
-llama70b (one Llama-3-70B layer, int8 G=256 and 6-bit G=32 round trips).
+llama70b (one Llama-3-70B layer, int8 G=256 and 6-bit G=32 round trips),
+qgz_two_hop (qgZ's reordered quantize and two-hop reduce, 2 nodes x 4 GPUs
+simulated), aquavit_schedule (the 1000-step ascending width schedule, in the
+metadata-interleaved and the planar layout) and ring_study (the ring
+reduce-scatter's hops against the one-hop reduce, with their errors).
 
 Timing: CUDA events on the launching stream, W untimed warm-up steps, then K
 timed steps bracketed by a barrier and a synchronize; the max over ranks is
@@ -17,7 +21,9 @@ step touches several GB (far more than the 126 MB L2) and no flush is needed.
 Inputs are seeded and synthetic (blockwise_quantized_zero_gb300.inputs).
 
 ``--impl reference`` times the oracle (plain single-threaded C) on a bounded
-sample of the same workload instead.
+sample of the same workload instead. The GPU run also times the oracle on one
+core (``cpu_baseline``) and on every host core (``cpu_baseline_all_cores``,
+one process per core).
 """
 from __future__ import annotations
 
@@ -1273,6 +1279,52 @@ def time_cpu_baseline(wl, sample):
             "sample": desc, "seconds": round(dt, 2)}
 
 
+def _oracle_core_worker(name, sample, barrier, queue):
+    """One process of the all-cores oracle timing: the unchanged single-threaded
+    oracle on `sample` elements of the workload, started together with the
+    other processes (host data only; no GPU)."""
+    try:
+        wl = WORKLOADS[name]()
+        run, nbytes, desc = _oracle_sample(wl, sample)
+        barrier.wait(timeout=900)
+        t0 = time.monotonic()
+        run()
+        queue.put((t0, time.monotonic(), nbytes, desc))
+    except Exception as e:  # reported by the parent
+        queue.put(("error", repr(e)))
+
+
+def time_cpu_all_cores(wl, sample):
+    """The oracle on every host core this process may use: one spawned process
+    per core, each on an equal share of the single-core sample (a whole copy of
+    it when the workload's sample is not an element count), started at a
+    barrier; the wall time runs from the first start to the last end."""
+    import inspect
+    import multiprocessing as mp
+
+    cores = len(os.sched_getaffinity(0))
+    if sample is None:
+        sample = inspect.signature(wl.oracle_sample).parameters["sample"].default
+    per = max(8192, (sample // cores) // 8192 * 8192) if isinstance(sample, int) else sample
+    ctx = mp.get_context("spawn")
+    barrier, queue = ctx.Barrier(cores), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_core_worker, args=(wl.name, per, barrier, queue))
+             for _ in range(cores)]
+    for p in procs:
+        p.start()
+    res = [queue.get(timeout=1800) for _ in procs]
+    for p in procs:
+        p.join()
+    bad = [r for r in res if r[0] == "error"]
+    if bad:
+        return {"error": bad[0][1], "cores": cores}
+    t0, t1 = min(r[0] for r in res), max(r[1] for r in res)
+    nbytes = sum(r[2] for r in res)
+    return {"value": round(nbytes / (t1 - t0) / 1e9, 4), "unit": UNIT, "cores": cores,
+            "kind": "oracle", "sample": f"{cores} processes, each: {res[0][3]}",
+            "seconds": round(t1 - t0, 2)}
+
+
 def run_gpu(args, rank, world, local):
     import torch
 
@@ -1389,6 +1441,8 @@ def run_gpu(args, rank, world, local):
     e2e_value = world * e2e_bytes * e2e_steps / e2e_t / 1e9
 
     cpu = time_cpu_baseline(wl, args.oracle_sample) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    cpu_all = (time_cpu_all_cores(wl, args.oracle_sample)
+               if (rank == 0 and world == 1 and not args.no_cpu) else None)
     if rank != 0:
         return None
     line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -1405,6 +1459,7 @@ def run_gpu(args, rank, world, local):
                          "us_per_launch": round(ms_sum / count * 1e3, 2)},
             "kernels": kernels,
             "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_all,
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": sum(l.kernels for l in launches) * args.steps,
