@@ -373,6 +373,45 @@ def pin_block_independence(lib):
             assert not np.any(cab[na + nb:])  # zero padding
 
 
+def pin_odd_symmetry(lib):
+    """Q(-x) = -Q(x): the scale depends on |x| only and rounding to nearest
+    with ties to even is symmetric about zero, so negating a block negates
+    every integer code (E4M3: flips every sign bit except of +0 codes) and
+    keeps the scale. Half-up rounding or a biased magic constant breaks it
+    on the exact half-steps included here."""
+    r = rng(51)
+    for fmt in ALL_FORMATS:
+        for G in (32, 128):
+            q = qmax(fmt) if fmt != O.E4M3 else 7
+            x = (r.standard_normal(4 * G) * 0.02).astype(np.float32)
+            x[:G] = ((np.arange(G) % (2 * q + 1)) - q + 0.5).astype(np.float32)  # half-steps
+            x[0] = np.float32(q)  # absmax q: scale 1, so the half-steps are exact ties
+            cp, sp = O.quantize(x, fmt, G, lib=lib)
+            cn, sn = O.quantize(-x, fmt, G, lib=lib)
+            assert np.array_equal(sp.view(np.uint32), sn.view(np.uint32)), (fmt, G)
+            if fmt == O.E4M3:
+                flip = np.where((cp & 0x7F) != 0, cp ^ 0x80, cp)
+                assert np.array_equal(cn, flip), (fmt, G)
+            else:
+                b = O.BITS[fmt]
+                assert np.array_equal(unpack_codes(cn, x.size, b), -unpack_codes(cp, x.size, b)), (fmt, G)
+
+
+def pin_power_of_two_scaling(lib):
+    """Q(2^k x): the block absmax, the scale and every quotient x/s scale by
+    2^k exactly (no rounding changes while nothing underflows or overflows),
+    so the codes are identical and the scales are 2^k times the originals."""
+    r = rng(52)
+    for fmt in ALL_FORMATS:
+        for G in (64, 1024):
+            x = (r.standard_normal(3 * G + 17) * 0.02).astype(np.float32)
+            c0, s0 = O.quantize(x, fmt, G, lib=lib)
+            for k in (-20, -3, 5, 40):
+                ck, sk = O.quantize((x * np.float32(2.0 ** k)).astype(np.float32), fmt, G, lib=lib)
+                assert np.array_equal(ck, c0), (fmt, G, k)
+                assert np.array_equal(sk, (s0 * np.float32(2.0 ** k)).astype(np.float32)), (fmt, G, k)
+
+
 def pin_roundtrip_bound(lib):
     """|x - D(Q(x))| <= s * (1/2 + 2^-22 * qmax) for integer codes with fp32 output;
     E4M3: |x - D| <= 2^-4 |x| + 2^-10 s + 2^-23 |x| (half an E4M3 ulp, plus rounding)."""
@@ -866,7 +905,8 @@ FAST_PINS = [
     pin_bpw_endpoints, pin_bpw_formula, pin_zeropp_payload, pin_bit_layout,
     pin_e4m3_points, pin_e4m3_vs_library, pin_f16_vs_library, pin_bf16_vs_library,
     pin_rounding_exhaustive_16bit, pin_rounding_fractions, pin_exact_multiples_and_ties,
-    pin_zero_and_tiny_blocks, pin_e4m3_quantize, pin_block_independence, pin_roundtrip_bound,
+    pin_zero_and_tiny_blocks, pin_e4m3_quantize, pin_block_independence, pin_odd_symmetry,
+    pin_power_of_two_scaling, pin_roundtrip_bound,
     pin_idempotence, pin_dequant_values, pin_reduce_single_shard, pin_reduce_pow2_exact,
     pin_reduce_order, pin_reduce_plain_sum_and_bound, pin_reduce_two_roundings,
     pin_fp8_reduce_no_overflow, pin_fp8_accumulate, pin_fp8_accumulate_two_roundings,

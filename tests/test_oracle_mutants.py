@@ -19,6 +19,7 @@ SRC = os.path.join(os.path.dirname(O.__file__), "zq_oracle.c")
 # (name, text to find (must occur exactly once), replacement)
 MUTANTS = [
     ("round_half_away", "float q = nearbyintf(t); /* ties to even, R3 */", "float q = roundf(t);"),
+    ("round_half_up", "float q = nearbyintf(t); /* ties to even, R3 */", "float q = floorf(t + 0.5f);"),
     ("truncate_instead_of_round", "float q = nearbyintf(t); /* ties to even, R3 */", "float q = truncf(t);"),
     ("qmax_off_by_one", "else s = m / (float)int_qmax(fmt);", "else s = m / (float)(int_qmax(fmt) + 1);"),
     ("multiply_by_reciprocal", "float t = v[i] / s;      /* IEEE division, R4 */",
