@@ -486,6 +486,28 @@ def _shards(r, N, n, fmt, G, scale=1e-4):
     return out
 
 
+def pin_reduce_zero_shard_neutral(lib):
+    """An all-zero shard (zero codes, zero scales) inserted at any position
+    changes nothing: every term it adds is +0, and a binary32 sum that
+    starts from +0 is unchanged by adding +0. A mean instead of a sum, or a
+    shard read at the wrong index, breaks this."""
+    r = rng(53)
+    n, G = 2 * 1024 + 77, 128
+    shards = _shards(r, 3, n, O.INT4, G)
+    zc = np.zeros_like(shards[0][0])
+    zs = np.zeros_like(shards[0][1])
+    base = O.reduce([c for c, _ in shards], [sc for _, sc in shards], n, O.INT4, G, O.INT8, 64,
+                    want_sum=True, lib=lib)
+    for pos in range(4):
+        cs = [c for c, _ in shards]
+        ss = [sc for _, sc in shards]
+        cs.insert(pos, zc)
+        ss.insert(pos, zs)
+        got = O.reduce(cs, ss, n, O.INT4, G, O.INT8, 64, want_sum=True, lib=lib)
+        assert np.array_equal(got[0], base[0]) and np.array_equal(got[1], base[1]), pos
+        assert np.array_equal(got[2].view(np.uint32), base[2].view(np.uint32)), pos
+
+
 def pin_reduce_single_shard(lib):
     """N = 1: the reduce is dequantize (fp32) followed by quantize."""
     r = rng(13)
@@ -907,7 +929,7 @@ FAST_PINS = [
     pin_rounding_exhaustive_16bit, pin_rounding_fractions, pin_exact_multiples_and_ties,
     pin_zero_and_tiny_blocks, pin_e4m3_quantize, pin_block_independence, pin_odd_symmetry,
     pin_power_of_two_scaling, pin_roundtrip_bound,
-    pin_idempotence, pin_dequant_values, pin_reduce_single_shard, pin_reduce_pow2_exact,
+    pin_idempotence, pin_dequant_values, pin_reduce_zero_shard_neutral, pin_reduce_single_shard, pin_reduce_pow2_exact,
     pin_reduce_order, pin_reduce_plain_sum_and_bound, pin_reduce_two_roundings,
     pin_fp8_reduce_no_overflow, pin_fp8_accumulate, pin_fp8_accumulate_two_roundings,
     pin_reordered_quantize_identity, pin_two_hop_ownership, pin_two_hop_exact_sums,
