@@ -156,6 +156,21 @@ def _cuda_contig(t, name):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _need(t, nbytes: int, name: str):
+    """t must be a contiguous CUDA tensor of at least nbytes bytes (the C ABI
+    takes raw pointers, so the binding refuses buffers the kernels would
+    overrun)."""
+    _cuda_contig(t, name)
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{name} holds {have} bytes; the call needs {nbytes}")
+
+
+def _need_pair(codes, scales, fmt: int, n: int, G: int, name: str):
+    _need(codes, codes_bytes(fmt, n), f"{name} codes")
+    _need(scales, 4 * num_blocks(n, G), f"{name} scales")
+
+
 def empty_codes(fmt: int, n: int, device):
     torch = _torch()
     return torch.empty(codes_bytes(fmt, n), dtype=torch.uint8, device=device)
@@ -172,6 +187,7 @@ def quantize(src, fmt: int, G: int, codes=None, scales=None, stream=None):
     n = src.numel()
     codes = empty_codes(fmt, n, src.device) if codes is None else codes
     scales = empty_scales(n, G, src.device) if scales is None else scales
+    _need_pair(codes, scales, fmt, n, G, "output")
     _check(lib().zq_quantize(src.data_ptr(), dtype_code(src.dtype), n, fmt, G, codes.data_ptr(),
                              scales.data_ptr(), _stream(src, stream)), "zq_quantize")
     return codes, scales
@@ -180,9 +196,10 @@ def quantize(src, fmt: int, G: int, codes=None, scales=None, stream=None):
 def dequantize(codes, scales, n: int, fmt: int, G: int, out_dtype=None, out=None, stream=None):
     """Dequantize packed codes -> a CUDA tensor of n elements (default bf16)."""
     torch = _torch()
-    _cuda_contig(codes, "codes")
+    _need_pair(codes, scales, fmt, n, G, "input")
     if out is None:
         out = torch.empty(n, dtype=out_dtype or torch.bfloat16, device=codes.device)
+    _need(out, max(n, 0) * out.element_size(), "out")
     _check(lib().zq_dequantize(codes.data_ptr(), scales.data_ptr(), n, fmt, G, out.data_ptr(),
                                dtype_code(out.dtype), _stream(codes, stream)), "zq_dequantize")
     return out
@@ -204,6 +221,14 @@ def reduce_ring(codes_list, scales_list, n: int, fmt: int, G: int, fmt_out: int,
         sum_out = torch.empty(n, dtype=torch.float32, device=dev)
     if partials is None and N >= 3:
         partials = [(empty_codes(fmt, n, dev), empty_scales(n, G, dev)) for _ in range(2)]
+    for r in range(N):
+        _need_pair(codes_list[r], scales_list[r], fmt, n, G, f"shard {r}")
+    _need_pair(out_codes, out_scales, fmt_out, n, G_out, "output")
+    if sum_out is not None:
+        _need(sum_out, 4 * max(n, 0), "sum_out")
+    if partials and N >= 3:
+        for k, (pc_, ps_) in enumerate(partials[:2]):
+            _need_pair(pc_, ps_, fmt, n, G, f"partial {k}")
     cp = (ctypes.c_void_p * N)(*[c.data_ptr() for c in codes_list])
     sp = (ctypes.c_void_p * N)(*[s.data_ptr() for s in scales_list])
     pc = (ctypes.c_void_p * 2)(*[c.data_ptr() for c, _ in partials]) if partials else None
@@ -228,6 +253,7 @@ def quantize_interleaved(src, fmt: int, G: int, records=None, stream=None):
     if records is None:
         records = torch.empty(max(interleaved_bytes(fmt, n, G), 1), dtype=torch.uint8,
                               device=src.device)
+    _need(records, interleaved_bytes(fmt, n, G), "records")
     _check(lib().zq_quantize_interleaved(src.data_ptr(), dtype_code(src.dtype), n, fmt, G,
                                          records.data_ptr(), _stream(src, stream)),
            "zq_quantize_interleaved")
@@ -238,9 +264,10 @@ def dequantize_interleaved(records, n: int, fmt: int, G: int, out_dtype=None, ou
                            stream=None):
     """Dequantize a record stream -> a CUDA tensor of n elements (default bf16)."""
     torch = _torch()
-    _cuda_contig(records, "records")
+    _need(records, interleaved_bytes(fmt, n, G), "records")
     if out is None:
         out = torch.empty(n, dtype=out_dtype or torch.bfloat16, device=records.device)
+    _need(out, max(n, 0) * out.element_size(), "out")
     _check(lib().zq_dequantize_interleaved(records.data_ptr(), n, fmt, G, out.data_ptr(),
                                            dtype_code(out.dtype), _stream(records, stream)),
            "zq_dequantize_interleaved")
@@ -268,6 +295,11 @@ def _reduce(entry: str, codes_list, scales_list, n, fmt_in, G_in, fmt_out, G_out
     out_scales = empty_scales(n, G_out, dev) if out_scales is None else out_scales
     if sum_out is True:
         sum_out = torch.empty(n, dtype=torch.float32, device=dev)
+    for r in range(N):
+        _need_pair(codes_list[r], scales_list[r], fmt_in, n, G_in, f"shard {r}")
+    _need_pair(out_codes, out_scales, fmt_out, n, G_out, "output")
+    if sum_out is not None:
+        _need(sum_out, 4 * max(n, 0), "sum_out")
     cp = (ctypes.c_void_p * N)(*[c.data_ptr() for c in codes_list])
     sp = (ctypes.c_void_p * N)(*[s.data_ptr() for s in scales_list])
     _check(getattr(lib(), entry)(cp, sp, N, n, fmt_in, G_in, out_codes.data_ptr(),
@@ -284,6 +316,7 @@ def quantize_reordered(src, fmt: int, G: int, nodes: int, gpus_per_node: int, co
     n = src.numel()
     codes = empty_codes(fmt, n, src.device) if codes is None else codes
     scales = empty_scales(n, G, src.device) if scales is None else scales
+    _need_pair(codes, scales, fmt, n, G, "output")
     _check(lib().zq_quantize_reordered(src.data_ptr(), dtype_code(src.dtype), n, fmt, G, nodes,
                                        gpus_per_node, codes.data_ptr(), scales.data_ptr(),
                                        _stream(src, stream)), "zq_quantize_reordered")
@@ -310,6 +343,14 @@ def reduce_two_hop(codes_list, scales_list, nodes: int, gpus_per_node: int, n: i
         out = [(empty_codes(fmt_out, m, dev), empty_scales(m, G_out, dev)) for _ in range(P)]
     if sums is True:
         sums = [torch.empty(m, dtype=torch.float32, device=dev) for _ in range(P)]
+    if len(mid) != P or len(out) != P or (sums is not None and len(sums) != P):
+        raise ValueError("need one mid, out (and sums) buffer per GPU")
+    for g in range(P):
+        _need_pair(codes_list[g], scales_list[g], fmt_in, n, G_in, f"GPU {g} input")
+        _need_pair(mid[g][0], mid[g][1], fmt_mid, nodes * m, G_mid, f"GPU {g} mid")
+        _need_pair(out[g][0], out[g][1], fmt_out, m, G_out, f"GPU {g} output")
+        if sums is not None:
+            _need(sums[g], 4 * max(m, 0), f"GPU {g} sums")
 
     def arr(ts):
         return (ctypes.c_void_p * P)(*[t.data_ptr() for t in ts])
@@ -348,6 +389,7 @@ def reduce_quantized_static(codes_list, scales_list, n: int, fmt_in: int, G_in: 
 def fp8_accumulate(main_codes, main_scales, grad, G: int, stream=None):
     """In place: main (E4M3 codes + scales) <- Q8(D8(main) + grad)."""
     _cuda_contig(grad, "grad")
+    _need_pair(main_codes, main_scales, E4M3, grad.numel(), G, "main")
     _check(lib().zq_fp8_accumulate(main_codes.data_ptr(), main_scales.data_ptr(), grad.data_ptr(),
                                    dtype_code(grad.dtype), grad.numel(), G,
                                    _stream(grad, stream)), "zq_fp8_accumulate")
