@@ -640,6 +640,24 @@ def pin_fp8_accumulate(lib):
         assert np.all(np.abs(now - v) <= 2.0 ** -4 * np.abs(v) + 2.0 ** -10 * ss + 2.0 ** -20 * np.abs(v))
 
 
+def pin_fp8_accumulate_cancellation(lib):
+    """Adding the exact negation of the dequantized main gradient (an fp32
+    gradient) cancels every element: fl(d + (-d)) = +0, the block absmax is
+    0, so every scale is 0 and every code 0x00. The dequantized values d are
+    recomputed here from torch's E4M3 decoding and one binary32 product."""
+    import torch
+
+    r = rng(54)
+    n, G = 4096, 128
+    g0 = torch_bf16_bits((r.standard_normal(n) * 1e-3).astype(np.float32))
+    c, s = O.fp8_accumulate(np.zeros(n, np.uint8), np.zeros(n // G, np.float32), g0, G,
+                            grad_dtype=O.BF16, lib=lib)
+    e = torch.from_numpy(c.copy()).view(torch.float8_e4m3fn).float().numpy()
+    d = (e * np.repeat(s, G)).astype(np.float32)  # one binary32 product each
+    c2, s2 = O.fp8_accumulate(c, s, -d, G, grad_dtype=O.F32, lib=lib)
+    assert not np.any(c2) and not np.any(s2.view(np.uint32))
+
+
 def pin_fp8_accumulate_two_roundings(lib):
     """v = fl(fl(D8(c) * s) + g): with D8 = 9/8, s = 1 + 2^-22 and g = -9/8 the
     product rounds to 9/8 + 2^-22, so v = 2^-22 (a fused form gives 9 * 2^-25),
@@ -931,7 +949,7 @@ FAST_PINS = [
     pin_power_of_two_scaling, pin_roundtrip_bound,
     pin_idempotence, pin_dequant_values, pin_reduce_zero_shard_neutral, pin_reduce_single_shard, pin_reduce_pow2_exact,
     pin_reduce_order, pin_reduce_plain_sum_and_bound, pin_reduce_two_roundings,
-    pin_fp8_reduce_no_overflow, pin_fp8_accumulate, pin_fp8_accumulate_two_roundings,
+    pin_fp8_reduce_no_overflow, pin_fp8_accumulate, pin_fp8_accumulate_cancellation, pin_fp8_accumulate_two_roundings,
     pin_reordered_quantize_identity, pin_two_hop_ownership, pin_two_hop_exact_sums,
     pin_two_hop_order, pin_il_size, pin_il_hand_records, pin_il_is_a_regrouping,
     pin_schedule_closed_forms, pin_schedule_pick, pin_ring_small_n, pin_ring_exact_sums,
