@@ -1,18 +1,25 @@
 """Benchmark of the blockwise quantize / pack / dequantize / reduce path on GB300.
 
-One JSON line (rank 0) per run. Default workload (``--workload gm_sweep``):
-granularity-modulation sweep on one 8192x8192 bf16 weight shard ~ N(0, 0.02):
-for every b in {2,4,6,8} and G in {1024,...,32}, quantize then dequantize to
-bf16 (48 kernel launches per step). Metric: GB/s of algorithmic input+output
-bytes. Other workloads (``--workload``): qwz_fp16 (1 Mi fp16 weights with
-outliers, int8 G=256, batched over 512 tensors), qgz_reduce (8 int4 shards of
-134,217,728 gradients -> int4 G=128 and int8 G=256), agoq_fp8 (E4M3 main
-gradient of 268,435,456 elements, 4 accumulate steps + 8-shard FP8 reduce),
-llama70b (one Llama-3-70B layer, int8 G=256 and 6-bit G=32 round trips),
-qgz_two_hop (qgZ's reordered quantize and two-hop reduce, 2 nodes x 4 GPUs
-simulated), aquavit_schedule (the 1000-step ascending width schedule, in the
-metadata-interleaved and the planar layout) and ring_study (the ring
-reduce-scatter's hops against the one-hop reduce, with their errors).
+One JSON line (rank 0) per run. Default workload (``--workload llama70b``,
+the largest single-GPU configuration): one Llama-3-70B decoder layer's bf16
+weights (q, o 8192x8192; k, v 8192x1024; gate, up 8192x28672; down
+28672x8192; 855,638,016 elements ~ N(0, 0.02)) quantized to int8 G=256 and to
+6-bit G=32, then dequantized to bf16 (28 launches per step). Metric: GB/s of
+algorithmic input+output bytes. The same run then times the kernel families
+of the other configurations (``--configs``, reported under ``configs``):
+qwz_fp16 (1 Mi fp16 weights with outliers, int8 G=256, batched over 512
+tensors), gm_sweep (8192x8192 bf16, b in {2,4,6,8} x G in {1024..32}),
+qgz_reduce (8 int4 shards of 134,217,728 gradients -> int4 G=128 and int8
+G=256) and agoq_fp8 (E4M3 main gradient of 268,435,456 elements, 4 accumulate
+steps + 8-shard FP8 reduce). Further workloads (``--workload``): qgz_two_hop
+(qgZ's reordered quantize and two-hop reduce, 2 nodes x 4 GPUs simulated),
+aquavit_schedule (the 1000-step ascending width schedule, in the metadata-
+interleaved and the planar layout) and ring_study (the ring reduce-scatter's
+hops against the one-hop reduce, with their errors).
+
+After every timed region the library's device error words are read
+(zq_device_status); if a bounded device-side wait ran out, no number is
+printed and the run exits non-zero.
 
 Timing: CUDA events on the launching stream, W untimed warm-up steps, then K
 timed steps bracketed by a barrier and a synchronize; the max over ranks is
@@ -1325,15 +1332,51 @@ def time_cpu_all_cores(wl, sample):
             "seconds": round(t1 - t0, 2)}
 
 
-def run_gpu(args, rank, world, local):
+# The configurations timed after the headline workload in the same run (the
+# other single-GPU workloads of the method: the batched 1 Mi fp16 round trip,
+# the granularity sweep, the qgZ reduce and the AGoQ FP8 accumulate + reduce).
+EXTRA_CONFIGS = ("qwz_fp16", "gm_sweep", "qgz_reduce", "agoq_fp8")
+EXTRA_STEPS = 20  # timed steps per extra configuration (at most --steps)
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, the ~8 TB/s nominal figure
+
+
+def check_device(zq, what: str):
+    """Refuse to report a number measured while a bounded device-side wait ran
+    out (the kernels' outputs would then be incomplete)."""
+    try:
+        zq.device_status()
+    except zq.ZQError as e:
+        raise SystemExit(f"bench.py: {what}: {e}; a bounded device-side wait ran out, so no "
+                         "number is reported") from None
+
+
+def _groups(launches):
+    """Maximal runs of consecutive launches of one kernel family."""
+    groups = []
+    for i, l in enumerate(launches):
+        if groups and groups[-1][0] == l.family:
+            groups[-1][1].append(i)
+        else:
+            groups.append((l.family, [i]))
+    return groups
+
+
+def family_table(fam, peak):
+    return {k: {"gbs": round(v[1] / (v[0] / 1e3) / 1e9, 1),
+                "frac": round(v[1] / (v[0] / 1e3) / 1e9 / peak, 4),
+                "frac_of_nominal_hbm": round(v[1] / (v[0] / 1e3) / 1e9 / NOMINAL_HBM_GBS, 4),
+                "bytes_per_launch": int(v[1] / v[2]),
+                "us_per_launch": round(v[0] / v[2] * 1e3, 2), "launches": v[2]}
+            for k, v in fam.items()}
+
+
+def time_steps(launches, steps, world, stream, per_launch=True):
+    """Time `steps` steps of `launches` in up to three regions (see run_gpu).
+    Returns (elapsed seconds of the back-to-back region, max over ranks;
+    per-family [ms, bytes, launches]; per-label [ms, bytes, count] or None)."""
     import torch
 
-    torch.cuda.set_device(local)
-    wl = make_workload(args)
-    wl.setup()
-    launches = wl.launches()
-    stream = torch.cuda.current_stream()
-    step_bytes = sum(l.nbytes for l in launches)
+    groups = _groups(launches)
 
     def step(evs=None):
         for i, l in enumerate(launches):
@@ -1343,75 +1386,118 @@ def run_gpu(args, rank, world, local):
             if evs is not None:
                 evs[i][1].record(stream)
 
-    for _ in range(args.warmup):
-        step()
+    def ev():
+        return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    gevs = [[ev() for _ in groups] for _ in range(steps)]
+    evs = [[ev() for _ in launches] for _ in range(steps)] if per_launch else None
+    t_start, t_end = ev()
+    barrier(world)
     torch.cuda.synchronize()
-
-    # Three timed regions of K steps each. The first runs the launches back to
-    # back, as a user's stream does (the kernels use programmatic dependent
-    # launch, which an event recorded between two launches would defeat): it
-    # gives `value`. The second records events only where the kernel family
-    # changes, so each family's launches still run back to back: its group
-    # times give each family's average launch duration for the roofline. The
-    # third brackets every launch with an event pair, for the per-launch table
-    # (isolated launches, so it includes each launch's start-up).
-    groups = []  # maximal runs of consecutive launches of one family
-    for i, l in enumerate(launches):
-        if groups and groups[-1][0] == l.family:
-            groups[-1][1].append(i)
-        else:
-            groups.append((l.family, [i]))
-    gevs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in groups] for _ in range(args.steps)]
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in launches] for _ in range(args.steps)]
-
-    def step_groups(gev):
+    t_start.record(stream)
+    for _ in range(steps):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    for k in range(steps):
         for gi, (_, idx) in enumerate(groups):
-            gev[gi][0].record(stream)
+            gevs[k][gi][0].record(stream)
             for i in idx:
                 launches[i].fn()
-            gev[gi][1].record(stream)
-
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
-        barrier(world)
-        torch.cuda.synchronize()
-        t_start.record(stream)
-        for k in range(args.steps):
-            step()
-        t_end.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        for k in range(args.steps):
-            step_groups(gevs[k])
-        torch.cuda.synchronize()
-        barrier(world)
-        for k in range(args.steps):
+            gevs[k][gi][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    if per_launch:
+        for k in range(steps):
             step(evs[k])
         torch.cuda.synchronize()
         barrier(world)
-    elapsed = t_start.elapsed_time(t_end) / 1e3
-    elapsed_max = max_over_ranks(elapsed, world)
-    value, _ = aggregate(step_bytes * args.steps, [elapsed_max], world)
-
-    # per-kernel-family durations (launches of a family back to back)
+    elapsed = max_over_ranks(t_start.elapsed_time(t_end) / 1e3, world)
     fam = {}
-    for k in range(args.steps):
+    for k in range(steps):
         for gi, (family, idx) in enumerate(groups):
             f = fam.setdefault(family, [0.0, 0, 0])
             f[0] += gevs[k][gi][0].elapsed_time(gevs[k][gi][1])
             f[1] += sum(launches[i].nbytes for i in idx)
             f[2] += sum(launches[i].kernels for i in idx)
-    # per-launch durations (each launch bracketed by events)
-    per_label = {}
-    for k in range(args.steps):
-        for i, l in enumerate(launches):
-            ms = evs[k][i][0].elapsed_time(evs[k][i][1])
-            pl = per_label.setdefault(l.label, [0.0, 0, 0])
-            pl[0] += ms
-            pl[1] += l.nbytes
-            pl[2] += 1
+    per_label = None
+    if per_launch:
+        per_label = {}
+        for k in range(steps):
+            for i, l in enumerate(launches):
+                pl = per_label.setdefault(l.label, [0.0, 0, 0])
+                pl[0] += evs[k][i][0].elapsed_time(evs[k][i][1])
+                pl[1] += l.nbytes
+                pl[2] += 1
+    return elapsed, fam, per_label
+
+
+def run_extra_config(name, args, world):
+    """Set up one more workload, time its kernel families (same protocol as the
+    headline, fewer steps), check the device error words, free it."""
+    import torch
+
+    import blockwise_quantized_zero_gb300 as zq
+
+    t0 = time.perf_counter()
+    wl = WORKLOADS[name]()
+    wl.setup()
+    launches = wl.launches()
+    stream = torch.cuda.current_stream()
+    steps = max(1, min(args.steps, EXTRA_STEPS))
+    for _ in range(args.warmup):
+        for l in launches:
+            l.fn()
+    torch.cuda.synchronize()
+    elapsed, fam, _ = time_steps(launches, steps, world, stream, per_launch=False)
+    check_device(zq, name)
+    peak, _ = measured_peak()
+    step_bytes = sum(l.nbytes for l in launches)
+    value, _ = aggregate(step_bytes * steps, [elapsed], world)
+    out = {"config": wl.config(), "value": round(value, 2), "unit": UNIT,
+           "frac": round(value / peak, 4), "steps": steps, "warmup": args.warmup,
+           "ms_per_step": round(elapsed / steps * 1e3, 3),
+           "families": family_table(fam, peak),
+           "gpu_launches": sum(l.kernels for l in launches) * steps,
+           "device_status": "ok", "wall_s": None}
+    del launches, wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    out["wall_s"] = round(time.perf_counter() - t0, 1)
+    return out
+
+
+def run_gpu(args, rank, world, local):
+    import torch
+
+    import blockwise_quantized_zero_gb300 as zq
+
+    torch.cuda.set_device(local)
+    wl = make_workload(args)
+    wl.setup()
+    launches = wl.launches()
+    stream = torch.cuda.current_stream()
+    step_bytes = sum(l.nbytes for l in launches)
+    for _ in range(args.warmup):
+        for l in launches:
+            l.fn()
+    torch.cuda.synchronize()
+    check_device(zq, f"{wl.name} warm-up")
+
+    # Three timed regions of K steps each (time_steps). The first runs the
+    # launches back to back, as a user's stream does (the kernels use
+    # programmatic dependent launch, which an event recorded between two
+    # launches would defeat): it gives `value`. The second records events only
+    # where the kernel family changes, so each family's launches still run back
+    # to back: its group times give each family's average launch duration for
+    # the roofline. The third brackets every launch with an event pair, for the
+    # per-launch table (isolated launches, so it includes each launch's start-up).
+    with ClockSampler(local) as clocks:
+        elapsed_max, fam, per_label = time_steps(launches, args.steps, world, stream)
+    check_device(zq, f"{wl.name} timed steps")
+    value, _ = aggregate(step_bytes * args.steps, [elapsed_max], world)
+
     dominant = max(fam, key=lambda k: fam[k][0])
     peak, peak_src = measured_peak()
     ms_sum, nbytes, count = fam[dominant]
@@ -1436,9 +1522,21 @@ def run_gpu(args, rank, world, local):
         wl.e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
+    check_device(zq, f"{wl.name} end-to-end steps")
     e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
     e2e_bytes = wl.e2e_bytes() if hasattr(wl, "e2e_bytes") else step_bytes
     e2e_value = world * e2e_bytes * e2e_steps / e2e_t / 1e9
+    main_config = wl.config()
+    gpu_launches = sum(l.kernels for l in launches) * args.steps
+    del launches
+
+    # the other configurations of the method, timed in the same run
+    extra = {}
+    names = [] if args.configs in ("", "none") else [c for c in args.configs.split(",") if c]
+    for name in names:
+        if name not in WORKLOADS or name == args.workload:
+            continue
+        extra[name] = run_extra_config(name, args, world)
 
     cpu = time_cpu_baseline(wl, args.oracle_sample) if (rank == 0 and world == 1 and not args.no_cpu) else None
     cpu_all = (time_cpu_all_cores(wl, args.oracle_sample)
@@ -1450,11 +1548,15 @@ def run_gpu(args, rank, world, local):
             "ms_per_step": round(elapsed_max / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
             "data": "synthetic (seeded, blockwise_quantized_zero_gb300.inputs)",
-            "config": dict(wl.config(), parallelism=f"replicas x{world} (no collective)"),
+            "config": dict(main_config, parallelism=f"replicas x{world} (no collective)"),
             "frac_of_peak": round(value / peak, 4),
+            "frac_of_nominal_hbm": round(value / NOMINAL_HBM_GBS, 4),
             "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1),
                          "peak": peak, "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)",
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "frac_of_nominal_hbm": round(achieved / NOMINAL_HBM_GBS, 4),
+                         "nominal_hbm_gbs": NOMINAL_HBM_GBS,
+                         "target_uses": "frac (of the measured copy peak)",
                          "algorithmic_bytes_per_launch": int(nbytes / count),
                          "us_per_launch": round(ms_sum / count * 1e3, 2)},
             "kernels": kernels,
@@ -1462,14 +1564,14 @@ def run_gpu(args, rank, world, local):
             "cpu_baseline_all_cores": cpu_all,
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-            "gpu_launches": sum(l.kernels for l in launches) * args.steps,
+            "gpu_launches": gpu_launches,
             "gpu_launches_note": "per timed region (the value's); two more regions of as many "
                                  "launches time the kernel families (events only between "
-                                 "families) and each launch alone (the kernels table)",
-            "families": {k: {"gbs": round(v[1] / (v[0] / 1e3) / 1e9, 1),
-                             "frac": round(v[1] / (v[0] / 1e3) / 1e9 / peak, 4),
-                             "us_per_launch": round(v[0] / v[2] * 1e3, 2), "launches": v[2]}
-                         for k, v in fam.items()},
+                                 "families) and each launch alone (the kernels table); the "
+                                 "configs entries count their own launches",
+            "families": family_table(fam, peak),
+            "configs": extra,
+            "device_status": "ok (checked after every timed region)",
             "clocks": clocks.summary()}
     return line
 
@@ -1506,7 +1608,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["zq", "reference"], default="zq")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gm_sweep")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama70b")
+    ap.add_argument("--configs", default=",".join(EXTRA_CONFIGS),
+                    help="comma-separated workloads whose kernel families are also timed in the "
+                         "same run (default: the other single-GPU configurations; 'none' to skip)")
     ap.add_argument("--oracle-sample", type=int, default=None,
                     help="elements in the CPU-oracle sample (default: the workload's own)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")

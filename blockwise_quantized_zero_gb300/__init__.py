@@ -67,6 +67,8 @@ def _declare(L):
     L.zq_reduce_quantized_static.argtypes = [vp, vp, i32, i64, i32, i64, vp, vp, i32, i64, vp, vp]
     L.zq_reduce_quantized_static.restype = i32
     L.zq_fp8_accumulate.argtypes = [vp, vp, vp, i32, i64, i64, vp]
+    L.zq_wait_selftest.argtypes = [i64, vp]
+    L.zq_wait_selftest.restype = i32
     for f in ("zq_quantize", "zq_dequantize", "zq_reduce_quantized", "zq_fp8_accumulate"):
         getattr(L, f).restype = i32
     L.zq_interleaved_bytes.argtypes = [i32, i64, i64]
@@ -402,3 +404,13 @@ def device_status(stream=None):
     torch = _torch()
     st = stream if stream is not None else torch.cuda.current_stream()
     _check(lib().zq_device_status(ctypes.c_void_p(st.cuda_stream)), "zq_device_status")
+
+
+def wait_selftest(limit_us: int = 5000, stream=None):
+    """Enqueue the bounded-wait self-test (zq_wait_selftest): a kernel whose
+    waits on a barrier that nothing completes run out after limit_us, so the
+    next device_status() raises ZQError(ZQ_ERR_TIMEOUT)."""
+    torch = _torch()
+    st = stream if stream is not None else torch.cuda.current_stream()
+    _check(lib().zq_wait_selftest(int(limit_us), ctypes.c_void_p(st.cuda_stream)),
+           "zq_wait_selftest")

@@ -173,6 +173,11 @@ int64_t zq_num_blocks(int64_t n, int64_t G) {
   return (n + G - 1) / G;
 }
 
+zq_status zq_wait_selftest(int64_t limit_us, void *stream) {
+  if (limit_us < 1 || limit_us > 100000) return ZQ_ERR_INVALID_ARG;
+  return from_cuda(launch_wait_selftest(uint64_t(limit_us) * 1000u, as_stream(stream)));
+}
+
 const char *zq_status_string(int status) {
   switch (status) {
     case ZQ_OK: return "ok";
@@ -552,6 +557,12 @@ zq_status zq_reduce_quantized_static(const void *const *codes, const float *cons
                                   G_in, out_codes, out_scales, format_out, G_out, sum_out))
     return st;
   if (n == 0) return ZQ_OK;
+  // The table is filled by copies from the caller's host arrays, which a
+  // captured graph would replay from memory the caller has since reused:
+  // refuse while the stream is being captured, with nothing enqueued.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaError_t e = cudaStreamIsCapturing(as_stream(stream), &cap)) return from_cuda(e);
+  if (cap != cudaStreamCaptureStatusNone) return ZQ_ERR_INVALID_ARG;
 
   TableReduceArgs a;
   std::memset(&a, 0, sizeof(a));

@@ -101,6 +101,8 @@ cudaError_t launch_reduce_static(const void *const *codes, const float *const *s
 // kFewShards shards).
 cudaError_t launch_reduce_few(const ReduceArgs &a, int fin, int fout, cudaStream_t st);
 cudaError_t launch_reduce_hop_few(const HopArgs &a, int fin, int fout, cudaStream_t st);
+// The bounded-wait self-test (a wait that nothing completes, limit_ns long).
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t st);
 // Reads and clears the device error words of the launch units.
 unsigned take_reduce_device_error();
 unsigned take_reduce_few_device_error();

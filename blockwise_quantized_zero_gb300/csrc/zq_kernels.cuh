@@ -106,8 +106,9 @@ struct SliceRemap {
   }
 };
 
-// Block scales of one tile. Lane l computes the scale (IEEE division) and
-// its reciprocal for block l of the tile (there are 1024 / G <= 32 blocks),
+// Block scales of one tile. Lane l computes the scale (block_scale: the
+// division-free remainder-corrected quotient, bit-identical to the IEEE
+// division absmax / qmax) and its reciprocal for block l of the tile (there are 1024 / G <= 32 blocks),
 // stores it, and the values are shuffled back to the lanes of each block.
 // m[j] is the lane's block absmax for run j (already reduced over the block).
 template <int FMT, int G, bool IL>
@@ -530,9 +531,10 @@ __device__ __forceinline__ void accumulate16(float (&acc)[kVec],
 
 // Requantize the sums of one tile of KU runs (KU*512 elements) with block
 // size 2^log2Gout (run time). As in quantize: the block absmax is a shuffle
-// tree over the G/16 lanes of a block; lane l then computes the scale (IEEE
-// division) and its reciprocal of block l of the tile, stores it, and the
-// lanes of each block fetch them back with a shuffle.
+// tree over the G/16 lanes of a block; lane l then computes the scale of
+// block l of the tile (block_scale: division-free, bit-identical to the IEEE
+// division) and its reciprocal, stores it, and the lanes of each block fetch
+// them back with a shuffle.
 template <int FOUT, int KU, typename A>
 __device__ __forceinline__ void requant_tile(const A &a, float (&acc)[KU][kVec],
                                              int64_t e0, int lane) {

@@ -40,10 +40,18 @@
  * ----------------------------------------------------------------------------
  *  - Every data pointer is a DEVICE pointer (memory the GPU can address, e.g.
  *    from cudaMalloc or a torch CUDA tensor), 16-byte aligned, owned by the
- *    caller. The library allocates nothing and never synchronizes: work is
- *    enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream)
- *    and the call returns. Pointer arrays (shards) are HOST arrays, read
- *    during the call only.
+ *    caller. The library allocates nothing, and no compute call waits for the
+ *    GPU: work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and the call returns. Two calls may block the host:
+ *    zq_device_status synchronizes the stream by design, and
+ *    zq_reduce_quantized_static copies the caller's host pointer arrays with
+ *    cudaMemcpyAsync, which for pageable host memory returns only once the
+ *    bytes are staged. Pointer arrays (shards) are HOST arrays, read during
+ *    the call only.
+ *  - Outputs are complete once the enqueued work has finished AND
+ *    zq_device_status has returned ZQ_OK for it: a reduce whose bounded
+ *    device-side wait ran out leaves its outputs undefined (see
+ *    zq_device_status).
  *  - Argument errors return synchronously with no work enqueued. A failed
  *    launch returns ZQ_ERR_CUDA; zq_last_cuda_error() then gives the CUDA
  *    runtime error code (per host thread). Errors that occur later on the
@@ -157,10 +165,17 @@ zq_status zq_reduce_quantized(const void *const *codes, const float *const *scal
  *   nshards   1 .. ZQ_STATIC_MAX_SHARDS; a larger count returns
  *             ZQ_ERR_INVALID_ARG with nothing enqueued.
  *   codes[r], scales[r]  HOST arrays, copied into the device table on `stream`
- *             (stream-ordered copies from host memory) during the call.
- * The first call on a device looks up the table's device address with
- * cudaGetSymbolAddress (with that device current); make that first call before
- * any stream capture. All calls share the one table: calls whose work overlaps
+ *             (stream-ordered copies from host memory) during the call; for
+ *             pageable host memory the call returns once they are staged.
+ *   stream    must not be capturing: the copies read the caller's host arrays,
+ *             which a replayed graph would read again after the caller has
+ *             reused them. A call on a capturing stream returns
+ *             ZQ_ERR_INVALID_ARG with nothing enqueued (and leaves the
+ *             capture intact).
+ * The first call in each CUDA context on a device looks up the table's device
+ * address with cudaGetSymbolAddress (with that device current) and caches it
+ * with the context handle; a new context (e.g. after cudaDeviceReset) is
+ * looked up again. All calls share the one table: calls whose work overlaps
  * on the GPU (e.g. on two streams that are not ordered) race on it and must not
  * be issued; calls on one stream are ordered and safe. It calls no cudaMalloc,
  * cudaFree or other allocating routine.
@@ -327,6 +342,20 @@ zq_status zq_fp8_accumulate(void *main_codes, float *main_scales, const void *gr
  * (A library-side check with no counterpart on the pages.)
  */
 zq_status zq_device_status(void *stream);
+
+/*
+ * zq_wait_selftest -- exercises the bounded device-side waits that
+ * zq_device_status reports (a library-side check with no counterpart on the
+ * pages). Enqueues one small kernel that waits, with the reduce kernels' own
+ * wait routines (the warp-wide wait of their consumer warps and the single-
+ * thread wait of their producer lane), on a shared-memory barrier that nothing
+ * completes, for limit_us microseconds each; both waits run out, set the
+ * timeout bit of the device error word and return. The next
+ * zq_device_status(stream) therefore returns ZQ_ERR_TIMEOUT (and clears the
+ * word); no output buffer is involved, and the CUDA context stays usable.
+ *   limit_us  1 .. 100000 (at most 0.1 s); otherwise ZQ_ERR_INVALID_ARG
+ */
+zq_status zq_wait_selftest(int64_t limit_us, void *stream);
 
 /* Static description of a status code. */
 const char *zq_status_string(int status);

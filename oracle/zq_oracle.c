@@ -366,8 +366,9 @@ static float dequant_elem(const uint8_t *codes, float s, int fmt, int64_t i)
 /* Public oracle entry points                                               */
 /* ------------------------------------------------------------------------ */
 
-/* One block of widened values (G <= 1024). */
-static float scratch[1024];
+/* Each entry point below keeps one block of widened values (G <= 1024) in a
+ * local array, so that independent calls may run on several host threads at
+ * once (the full-size parity tests split a tensor into whole-block chunks). */
 
 /* Quantize n elements of src (dtype) into packed codes and one scale per
  * block. codes must hold orc_codes_bytes(fmt, n) bytes, scales
@@ -375,6 +376,7 @@ static float scratch[1024];
 int orc_quantize(const void *src, int dtype, int64_t n, int fmt, int64_t G, uint8_t *codes,
                  float *scales)
 {
+    float scratch[1024];
     int64_t k, i, nb;
     if (!code_bits(fmt) || !valid_block(G) || !elem_size(dtype) || n < 0) return ORC_BAD;
     memset(codes, 0, (size_t)orc_codes_bytes(fmt, n));
@@ -404,6 +406,7 @@ int orc_reduce(const uint8_t *const *codes, const float *const *scales, int nsha
                int fmt_in, int64_t G_in, uint8_t *out_codes, float *out_scales, int fmt_out,
                int64_t G_out, float *sum_out)
 {
+    float scratch[1024];
     int64_t k, i, nb;
     int r;
     if (!code_bits(fmt_in) || !code_bits(fmt_out) || !valid_block(G_in) || !valid_block(G_out) ||
@@ -508,6 +511,7 @@ int orc_reduce_two_hop(const uint8_t *const *codes, const float *const *scales, 
 int orc_fp8_accumulate(uint8_t *codes, float *scales, const void *grad, int grad_dtype, int64_t n,
                        int64_t G)
 {
+    float scratch[1024];
     int64_t k, i, nb;
     if (!valid_block(G) || !elem_size(grad_dtype) || n < 0) return ORC_BAD;
     nb = orc_num_blocks(n, G);
@@ -573,6 +577,7 @@ int64_t orc_il_bytes(int fmt, int64_t n, int64_t G)
  * written at the start of its record and its codes after it. */
 int orc_quantize_interleaved(const void *src, int dtype, int64_t n, int fmt, int64_t G, uint8_t *rec)
 {
+    float scratch[1024];
     int64_t k, i, nb, pos = 0;
     if (orc_il_bytes(fmt, n, G) < 0 || !elem_size(dtype)) return ORC_BAD;
     memset(rec, 0, (size_t)orc_il_bytes(fmt, n, G));

@@ -223,3 +223,10 @@ def test_reduce_ring_argument_errors(L):
     assert r(pc=same) == ALIAS
     onto_out = (ctypes.c_void_p * 2)(oc, BASE + (1 << 33) + (1 << 20))
     assert r(pc=onto_out) == ALIAS
+
+
+def test_wait_selftest_limit_checked_before_the_device(L):
+    """The wait self-test accepts 1 .. 100000 microseconds; other limits are
+    refused before anything is enqueued (no device needed to see that)."""
+    for bad in (0, -1, 100001, 1 << 40):
+        assert L.zq_wait_selftest(bad, None) == INVALID

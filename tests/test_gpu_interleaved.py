@@ -114,28 +114,39 @@ def test_aquavit_schedule_run(zq):
     assert (O.INT2, 1024) in seen and (O.INT6, 32) in seen
 
 
-def test_full_shard_sampled_windows(zq):
+def test_full_shard_every_element(zq):
     """8192x8192 bf16 (the weight shard of the benchmark), every pair of the
-    schedule plus int8: windows of whole blocks checked against the oracle."""
+    schedule plus int8: every record and every dequantized value checked
+    against the oracle, chunk by chunk of whole blocks."""
+    import time
+
     import torch
 
+    import fullsize as F
     from blockwise_quantized_zero_gb300 import inputs
 
+    t0 = time.time()
     x = inputs.weight_shard_bf16()
     xd = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda()
     n = x.size
-    rng = np.random.default_rng(11)
-    starts = sorted({0, n - WIN} | set((rng.integers(0, (n - WIN) // 1024, 6) * 1024).tolist()))
+    total = 0
     for b in (2, 4, 6, 8):
         for G in BLOCKS:
             rec = zq.quantize_interleaved(xd, b, G)
             y = to_host(zq.dequantize_interleaved(rec, n, b, G, out_dtype=torch.bfloat16))
             hr = to_host(rec)
             R = 4 + G * b // 8
-            for lo in starts:
-                want = O.quantize_interleaved(x[lo:lo + WIN], b, G, dtype=O.BF16)
-                got = hr[(lo // G) * R:((lo + WIN) // G) * R]
-                assert np.array_equal(got, want), (b, G, lo)
-                wy = O.dequantize_interleaved(want, WIN, b, G, O.BF16)
-                assert np.array_equal(y[lo:lo + WIN], wy), (b, G, lo)
+
+            def chunk(span, b=b, G=G, R=R, hr=hr, y=y):
+                lo, hi = span
+                want = O.quantize_interleaved(np.ascontiguousarray(x[lo:hi]), b, G, dtype=O.BF16)
+                F.same(f"b={b} G={G}", "records", lo, hr[(lo // G) * R:(hi // G) * R], want)
+                wy = O.dequantize_interleaved(want, hi - lo, b, G, O.BF16)
+                F.same(f"b={b} G={G}", "dequantized values", lo, y[lo:hi], wy)
+                return hi - lo
+
+            total += sum(F.pmap(chunk, F.chunks(n)))
             del rec
+    assert total == 24 * n
+    print(f"\n[full-size parity] interleaved records: {total:,} elements compared bit for bit on "
+          f"{F.cores()} host cores in {time.time() - t0:.1f} s")

@@ -111,43 +111,75 @@ def test_two_hop_argument_errors(zq):
         zq.reduce_two_hop(c, s, A, L, n, O.INT4, 128, O.INT4, 128, O.INT4, 128, mid=mid, out=out)
 
 
-def test_two_hop_full_size_sampled(zq):
+def test_two_hop_full_size_every_element(zq):
     """The benchmark configuration (2 nodes x 4 GPUs, 134,217,728 fp32 per GPU,
-    int4 G=128 throughout), through the same calls the benchmark times. GPU
-    g's final chunk is the sum of chunk g of every gradient, so a window of
-    whole blocks of it follows from the same window of chunk g on every GPU:
-    the oracle quantizes those windows, sums them node by node (hop 1) and
-    over the nodes (hop 2), and must reproduce the GPU's codes, scales and
-    fp32 sums there."""
+    int4 G=128 throughout), through the same calls the benchmark times, on
+    every element: each GPU's reordered quantization, every hop-1 result and
+    every final chunk with its fp32 sums. The oracle quantizes each gradient
+    chunk by chunk (chunk c at its slice position), then, for each window of
+    whole blocks of final chunk g = a*L + l, sums that window of chunk g over
+    each node's GPUs in order (hop 1: the window of GPU (a2, l)'s hop-1 result
+    at chunk a) and over the nodes in order (hop 2)."""
+    import time
+
     import torch
 
+    import fullsize as F
     from blockwise_quantized_zero_gb300 import inputs
 
+    t0 = time.time()
     A, L, n, G = 2, 4, 134217728, 128
     P, m = A * L, n // (A * L)
-    hx, qd = [], []
+    qd, ref = [], []
     for g in range(P):
         x = inputs.gradient_shard_f32(n, shard=g)
-        xd = torch.from_numpy(x).cuda()
-        qd.append(zq.quantize_reordered(xd, O.INT4, G, A, L))
-        del xd
-        hx.append(x)
-    _, out, sums = zq.reduce_two_hop([c for c, _ in qd], [s for _, s in qd], A, L, n, O.INT4, G,
-                                     O.INT4, G, O.INT4, G, sums=True)
+        qd.append(zq.quantize_reordered(torch.from_numpy(x).cuda(), O.INT4, G, A, L))
+        codes = np.empty(O.codes_bytes(O.INT4, n), np.uint8)
+        scales = np.empty(n // G, np.float32)
+
+        def chunk(c):
+            pos = O.slice_position(c, A, L)
+            wc, ws = O.quantize(np.ascontiguousarray(x[c * m:(c + 1) * m]), O.INT4, G)
+            codes[pos * m // 2:(pos + 1) * m // 2] = wc
+            scales[pos * m // G:(pos + 1) * m // G] = ws
+
+        F.pmap(chunk, range(P))
+        F.same(f"GPU {g} reordered quantize", "codes", 0, to_host(qd[g][0]), codes)
+        F.same(f"GPU {g} reordered quantize", "scales", 0, to_host(qd[g][1]), scales)
+        ref.append((codes, scales))
+        del x
+    mid, out, sums = zq.reduce_two_hop([c for c, _ in qd], [s for _, s in qd], A, L, n, O.INT4, G,
+                                       O.INT4, G, O.INT4, G, sums=True)
     zq.device_status()
-    W = 4096
-    rng = np.random.default_rng(17)
-    for g, lo in [(0, 0), (P - 1, m - W)] + [(int(rng.integers(0, P)), int(rng.integers(0, (m - W) // G)) * G)
-                                             for _ in range(4)]:
-        win = [O.quantize(np.ascontiguousarray(hx[g2][g * m + lo:g * m + lo + W]), O.INT4, G)
-               for g2 in range(P)]
-        mid = []
-        for a2 in range(A):  # hop 1: node a2's GPUs in order
-            part = [win[a2 * L + l2] for l2 in range(L)]
-            mc, ms, _ = O.reduce([c for c, _ in part], [s for _, s in part], W, O.INT4, G, O.INT4, G)
-            mid.append((mc, ms))
-        wc, ws, wsum = O.reduce([c for c, _ in mid], [s for _, s in mid], W, O.INT4, G, O.INT4, G,
+    hmid = [(to_host(c), to_host(s)) for c, s in mid]
+    hout = [(to_host(c), to_host(s)) for c, s in out]
+    hsum = [to_host(s) for s in sums]
+
+    def window(job):
+        g, lo, hi = job
+        a, l = divmod(g, L)
+        w = hi - lo
+        mids = []
+        for a2 in range(A):  # hop 1 on node a2: its GPUs in order, slice position l*A + a
+            off = (l * A + a) * m + lo
+            part = [ref[a2 * L + l2] for l2 in range(L)]
+            mc, ms, _ = O.reduce([F.code_slice(c, O.INT4, off, off + w) for c, _ in part],
+                                 [s[off // G:(off + w) // G] for _, s in part], w, O.INT4, G,
+                                 O.INT4, G)
+            moff = a * m + lo  # in GPU (a2, l)'s hop-1 result
+            gm = hmid[a2 * L + l]
+            F.same(f"GPU {a2 * L + l} hop 1", "codes", moff, F.code_slice(gm[0], O.INT4, moff, moff + w), mc)
+            F.same(f"GPU {a2 * L + l} hop 1", "scales", moff, gm[1][moff // G:(moff + w) // G], ms)
+            mids.append((mc, ms))
+        wc, ws, wsum = O.reduce([c for c, _ in mids], [s for _, s in mids], w, O.INT4, G, O.INT4, G,
                                 want_sum=True)
-        _same(to_host(sums[g][lo:lo + W]), wsum, f"GPU {g} sums at {lo}")
-        _same(to_host(out[g][1][lo // G:(lo + W) // G]), ws, f"GPU {g} scales at {lo}")
-        _same(to_host(out[g][0][lo // 2:(lo + W) // 2]), wc, f"GPU {g} codes at {lo}")
+        F.same(f"GPU {g} hop 2", "fp32 sums", lo, hsum[g][lo:hi], wsum)
+        F.same(f"GPU {g} hop 2", "scales", lo, hout[g][1][lo // G:hi // G], ws)
+        F.same(f"GPU {g} hop 2", "codes", lo, F.code_slice(hout[g][0], O.INT4, lo, hi), wc)
+        return w
+
+    total = sum(F.pmap(window, [(g, lo, hi) for g in range(P) for lo, hi in F.chunks(m)]))
+    assert total == n
+    print(f"\n[full-size parity] qgz_two_hop: {P} reordered quantizations ({P * n:,} elements), "
+          f"{P} hop-1 results ({A * n:,}) and {P} final chunks ({n:,}) compared bit for bit on "
+          f"{F.cores()} host cores in {time.time() - t0:.1f} s")

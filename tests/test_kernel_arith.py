@@ -95,7 +95,9 @@ def test_newton_reciprocal_error_bound(e):
             y0 = np.nextafter(y0, F32(np.inf) if k > 0 else F32(0.0))
         y64 = y0.astype(F64)
         e32 = (1.0 - s64 * y64).astype(F32)     # 1 - s*y0 exact in float64, one rounding
-        r = (y64 + y64 * e32.astype(F64)).astype(F32)  # y0*e exact; sum exact in f64 (< 50 bits)
+        # r = RN(y0 + y0*e): y0*e is exact in float64 (24 x 24 bits), the sum
+        # is not (y0*e reaches 2^-70 below y0), so it is rounded once with TwoSum
+        r = _rn32_of_sum(y64, y64 * e32.astype(F64))
         rel = np.abs(r.astype(F64) * s64 - 1.0)
         worst = max(worst, float(rel.max()))
     assert worst <= 2.0 ** -24 * (1 + 2.0 ** -18), worst

@@ -86,3 +86,50 @@ def test_static_reduce_beyond_64_shards_matches_the_definition(zq):
         wc, ws, wsum = O.reduce([c for c, _ in sh], [s for _, s in sh], n, O.INT4, 128, O.INT4,
                                 128, want_sum=True)
         _same(got, (wc, ws, wsum), f"N={N}")
+
+
+def test_static_reduce_at_the_shard_limit(zq):
+    """ZQ_STATIC_MAX_SHARDS shards (every table slot, the last shard batch and
+    the table's end) on a small ragged tensor, against the definition."""
+    N, n = zq.STATIC_MAX_SHARDS, 1024 + 77
+    sh = _shards(N, n, O.INT2, 32, seed=90)
+    got = _call(zq, "zq_reduce_quantized_static", sh, n, O.INT2, 32, O.INT4, 64)
+    wc, ws, wsum = O.reduce([c for c, _ in sh], [s for _, s in sh], n, O.INT2, 32, O.INT4, 64,
+                            want_sum=True)
+    _same(got, (wc, ws, wsum), f"N={N}")
+
+
+def test_static_reduce_refuses_while_capturing(zq):
+    """A call on a stream that is being captured returns ZQ_ERR_INVALID_ARG with
+    nothing enqueued (its table copies would read the caller's host arrays again
+    at every replay); the capture itself stays valid, and the next ordinary
+    call works."""
+    import torch
+
+    n = 4096
+    sh = _shards(3, n, O.INT4, 128, seed=95)
+    codes = [bytes_dev(c) for c, _ in sh]
+    scales = [bytes_dev(s) for _, s in sh]
+    oc = torch.zeros(zq.codes_bytes(O.INT4, n), dtype=torch.uint8, device="cuda")
+    os_ = torch.zeros(zq.num_blocks(n, 128), dtype=torch.float32, device="cuda")
+    marker = torch.zeros(1, dtype=torch.float32, device="cuda")
+    cp = (ctypes.c_void_p * 3)(*[c.data_ptr() for c in codes])
+    sp = (ctypes.c_void_p * 3)(*[s.data_ptr() for s in scales])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+            status = zq.lib().zq_reduce_quantized_static(cp, sp, 3, n, O.INT4, 128, oc.data_ptr(),
+                                                         os_.data_ptr(), O.INT4, 128, None, st)
+            marker.add_(1.0)
+    assert status == 1, status  # ZQ_ERR_INVALID_ARG
+    g.replay()
+    torch.cuda.synchronize()
+    assert marker.item() == 1.0  # the rest of the capture replays
+    assert int(oc.count_nonzero()) == 0 and int(os_.count_nonzero()) == 0  # nothing was enqueued
+    got = zq.reduce_quantized_static(codes, scales, n, O.INT4, 128, O.INT4, 128)
+    zq.device_status()
+    wc, ws, _ = O.reduce([c for c, _ in sh], [s for _, s in sh], n, O.INT4, 128, O.INT4, 128)
+    assert np.array_equal(to_host(got[0]), wc) and np.array_equal(as_bits(to_host(got[1])), as_bits(ws))
