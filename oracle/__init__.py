@@ -85,6 +85,8 @@ def _declare(lib):
     lib.orc_decode_n.argtypes = [i32, vp, i64, vp]
     lib.orc_encode_n.restype = i32
     lib.orc_decode_n.restype = i32
+    lib.orc_gemm_dequant.argtypes = [vp, i64, i64, vp, vp, i32, i64, i64, vp, vp, i64, vp, vp]
+    lib.orc_gemm_dequant.restype = i32
     for name in ("orc_quantize", "orc_dequantize", "orc_reduce", "orc_fp8_accumulate",
                  "orc_quantize_interleaved", "orc_dequantize_interleaved"):
         getattr(lib, name).restype = i32
@@ -365,3 +367,26 @@ def bf16_decode(h: int, lib=None) -> float:
 
 def bf16_encode(x: float, lib=None) -> int:
     return int((lib or load()).orc_bf16_encode(x))
+
+
+def gemm_dequant(x_bf16: np.ndarray, M: int, K: int, codes: np.ndarray, scales: np.ndarray,
+                 fmt: int, G: int, N: int, rows=None, cols=None, lib=None):
+    """Dequant-fused GEMM reference (reading R16 of zq_oracle.c): returns (y, absy),
+    float64, for the listed output positions (all M x N, row-major, when rows and
+    cols are None): y = x W_hat^T exactly, absy = the sums of |products|."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    if rows is None:
+        rr, cc = np.meshgrid(np.arange(M, dtype=np.int64), np.arange(N, dtype=np.int64), indexing="ij")
+        rows, cols = rr.ravel(), cc.ravel()
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    y = np.zeros(rows.size, np.float64)
+    absy = np.zeros(rows.size, np.float64)
+    rc = lib.orc_gemm_dequant(_ptr(x), M, K, _ptr(codes), _ptr(scales), fmt, G, N, _ptr(rows),
+                              _ptr(cols), rows.size, _ptr(y), _ptr(absy))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return y, absy

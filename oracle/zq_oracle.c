@@ -91,6 +91,22 @@
  *      over the two terms [partial, shard r] -- and requantizes it; the
  *      first partial is shard 0 itself; the last hop keeps acc (the fp32
  *      result) and requantizes it to the output format.
+ *  R16 the dequantization fused into the GEMM that consumes the gathered
+ *      weights ([AGoQ] section "C. Kernel Fusion": quantization and
+ *      dequantization fused with the adjacent GEMMs, the quantize/dequantize
+ *      arithmetic on the CUDA cores and the GEMM on the tensor cores; [ZeRO++]
+ *      qwZ: the weights a layer uses are the dequantized gathered ones):
+ *      the weight matrix W (N x K, row-major) is held as the codes and scales
+ *      of its flattened form, blocks of G along each row (K a multiple of G);
+ *      the GEMM's weight operand is that matrix dequantized and rounded to
+ *      bf16 exactly as the dequantize with a bf16 output does,
+ *      W_hat = bf16(fl32(q * s)); the product is y = x W_hat^T for bf16
+ *      activations x (M x K, row-major), summed in full precision. The
+ *      oracle gives the exact sum (every product of two bf16 values is exact
+ *      in binary64, and binary64 accumulation of K terms errs by at most
+ *      K 2^-53 of the sum of magnitudes, far below any fp32 accumulation),
+ *      together with that sum of magnitudes, from which a caller derives the
+ *      error bound of an fp32 accumulation in any order.
  */
 #include <math.h>
 #include <stddef.h>
@@ -677,6 +693,41 @@ int orc_reduce_ring(const uint8_t *const *codes, const float *const *scales, int
             rc = orc_reduce(sc, ss, 2, n, fmt, G, out_codes, out_scales, fmt_out, G_out, sum_out);
         }
         if (rc != ORC_OK) return rc;
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dequantization fused into the consumer GEMM (reading R16)                */
+/* ------------------------------------------------------------------------ */
+
+/* For each of the `count` output positions (rows[i], cols[i]):
+ *   y[i]    = sum over k of x[rows[i]][k] * W_hat[cols[i]][k]   (exact, binary64)
+ *   absy[i] = sum over k of |x[rows[i]][k] * W_hat[cols[i]][k]|
+ * with W_hat[n][k] the bf16 rounding of the dequantized element n*K + k of
+ * the flattened weight (codes, scales in (fmt, G) layout). x holds M*K bf16
+ * bit patterns. Requires K to be a multiple of G. */
+int orc_gemm_dequant(const uint16_t *x, int64_t M, int64_t K, const uint8_t *codes,
+                     const float *scales, int fmt, int64_t G, int64_t N, const int64_t *rows,
+                     const int64_t *cols, int64_t count, double *y, double *absy)
+{
+    int64_t i, k;
+    if (!code_bits(fmt) || !valid_block(G) || M < 1 || N < 1 || K < 1 || K % G != 0 || count < 0)
+        return ORC_BAD;
+    for (i = 0; i < count; ++i) {
+        int64_t m = rows[i], n = cols[i];
+        double acc = 0.0, mag = 0.0;
+        if (m < 0 || m >= M || n < 0 || n >= N) return ORC_BAD;
+        for (k = 0; k < K; ++k) {
+            int64_t e = n * K + k;
+            float wf = dequant_elem(codes, scales[e / G], fmt, e);       /* fl32(q * s) */
+            double w = (double)orc_bf16_decode(orc_bf16_encode(wf));     /* then bf16 */
+            double a = (double)orc_bf16_decode(x[m * K + k]);
+            acc += a * w; /* exact product; binary64 sum */
+            mag += fabs(a * w);
+        }
+        y[i] = acc;
+        absy[i] = mag;
     }
     return ORC_OK;
 }

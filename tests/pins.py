@@ -941,6 +941,79 @@ def pin_ring_requantizes_partials(lib):
     assert rev[1] != 0.0
 
 
+# ---------------------------------------------------------------------------
+# The dequantization fused into the consumer GEMM (the oracle's reading R16)
+# ---------------------------------------------------------------------------
+
+def _int_weights(r, N, K, G, qmax_):
+    """An N x K integer matrix whose every G-block holds +-qmax: its block
+    scales are exactly 1, so the dequantized (and bf16) weights are the
+    integers themselves."""
+    W = r.integers(-qmax_, qmax_ + 1, size=(N, K)).astype(np.int64)
+    W[:, ::G] = qmax_ * np.where(r.random((N, K // G)) < 0.5, -1, 1)
+    return W
+
+
+def pin_gemm_small_integers(lib):
+    """Small-integer operands: every product and partial sum is an integer, so
+    y and the sums of magnitudes equal int64 matrix products of the integer
+    matrices built here (non-square, so a transposed operand fails)."""
+    r = rng(301)
+    for fmt, G in ((O.INT8, 32), (O.INT4, 64), (O.INT2, 128)):
+        M, N, K = 3, 5, 256
+        W = _int_weights(r, N, K, G, qmax(fmt))
+        X = r.integers(-16, 17, size=(M, K)).astype(np.int64)
+        codes, scales = O.quantize(W.astype(np.float32).ravel(), fmt, G, lib=lib)
+        assert np.all(scales == 1.0)
+        xb = torch_bf16_bits(X.astype(np.float32).ravel())
+        y, absy = O.gemm_dequant(xb, M, K, codes, scales, fmt, G, N, lib=lib)
+        assert np.array_equal(y.reshape(M, N), (X @ W.T).astype(np.float64))
+        assert np.array_equal(absy.reshape(M, N), (np.abs(X) @ np.abs(W).T).astype(np.float64))
+
+
+def pin_gemm_bf16_weights_exact_sum(lib):
+    """Random weights and activations: the weight operand is the bf16 rounding
+    (torch) of the fp32 product code * scale (numpy float32), the codes read
+    back from the bit stream by the pinned unpacking helper, and y is the
+    exact rational sum of the products."""
+    r = rng(302)
+    for fmt, G in ((O.INT4, 32), (O.INT8, 64), (O.E4M3, 32), (O.INT6, 64)):
+        M, N, K = 2, 3, 128
+        w32 = (r.standard_normal(N * K) * 0.02).astype(np.float32)
+        codes, scales = O.quantize(w32, fmt, G, lib=lib)
+        if fmt == O.E4M3:
+            import torch
+
+            q = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).float().numpy()
+        else:
+            q = unpack_codes(codes, N * K, O.BITS[fmt]).astype(np.float32)
+        wq = (q * np.repeat(scales, G)).astype(np.float32)
+        wb = bf16_to_f32(torch_bf16_bits(wq)).reshape(N, K)
+        xb = torch_bf16_bits(r.standard_normal(M * K).astype(np.float32))
+        X = bf16_to_f32(xb).reshape(M, K)
+        y, absy = O.gemm_dequant(xb, M, K, codes, scales, fmt, G, N, lib=lib)
+        for m in range(M):
+            for n in range(N):
+                exact = sum(Fraction(float(X[m, k])) * Fraction(float(wb[n, k])) for k in range(K))
+                assert abs(Fraction(float(y[m * N + n])) - exact) <= Fraction(2) ** -50 * abs(exact) + Fraction(2) ** -1000
+                mag = sum(abs(Fraction(float(X[m, k])) * Fraction(float(wb[n, k]))) for k in range(K))
+                assert abs(Fraction(float(absy[m * N + n])) - mag) <= Fraction(2) ** -50 * mag
+
+
+def pin_gemm_identity_gives_dequantized_weights(lib):
+    """x = I (M = K): y[m][n] is the bf16-dequantized weight element (n, m),
+    the pinned dequantize's output transposed; sampled positions only."""
+    r = rng(303)
+    K = N = 64
+    w32 = (r.standard_normal(N * K) * 0.02).astype(np.float32)
+    codes, scales = O.quantize(w32, O.INT4, 32, lib=lib)
+    wd = bf16_to_f32(O.dequantize(codes, scales, N * K, O.INT4, 32, O.BF16, lib=lib)).reshape(N, K)
+    xb = torch_bf16_bits(np.eye(K, dtype=np.float32).ravel())
+    rows, cols = r.integers(0, K, 200), r.integers(0, N, 200)
+    y, _ = O.gemm_dequant(xb, K, K, codes, scales, O.INT4, 32, N, rows=rows, cols=cols, lib=lib)
+    assert np.array_equal(y, wd[cols, rows].astype(np.float64))
+
+
 FAST_PINS = [
     pin_bpw_endpoints, pin_bpw_formula, pin_zeropp_payload, pin_bit_layout,
     pin_e4m3_points, pin_e4m3_vs_library, pin_f16_vs_library, pin_bf16_vs_library,
@@ -953,5 +1026,6 @@ FAST_PINS = [
     pin_reordered_quantize_identity, pin_two_hop_ownership, pin_two_hop_exact_sums,
     pin_two_hop_order, pin_il_size, pin_il_hand_records, pin_il_is_a_regrouping,
     pin_schedule_closed_forms, pin_schedule_pick, pin_ring_small_n, pin_ring_exact_sums,
-    pin_ring_requantizes_partials,
+    pin_ring_requantizes_partials, pin_gemm_small_integers, pin_gemm_bf16_weights_exact_sum,
+    pin_gemm_identity_gives_dequantized_weights,
 ]

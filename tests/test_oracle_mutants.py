@@ -113,6 +113,14 @@ MUTANTS = [
     ("ring_partial_in_another_format",
      "rc = orc_reduce(sc, ss, 2, n, fmt, G, pc[r % 2], ps[r % 2], fmt, G, 0);",
      "rc = orc_reduce(sc, ss, 2, n, fmt, G, pc[r % 2], ps[r % 2], fmt == ORC_INT8 ? ORC_E4M3 : fmt, G, 0);"),
+    ("gemm_transposed_weight", "int64_t e = n * K + k;", "int64_t e = k * N + n;"),
+    ("gemm_no_bf16_rounding", "double w = (double)orc_bf16_decode(orc_bf16_encode(wf));",
+     "double w = (double)wf;"),
+    ("gemm_scale_of_row_start", "float wf = dequant_elem(codes, scales[e / G], fmt, e);",
+     "float wf = dequant_elem(codes, scales[(n * K) / G], fmt, e);"),
+    ("gemm_column_major_activations", "double a = (double)orc_bf16_decode(x[m * K + k]);",
+     "double a = (double)orc_bf16_decode(x[k * M + m < M * K ? k * M + m : 0]);"),
+    ("gemm_signed_magnitudes", "mag += fabs(a * w);", "mag += a * w;"),
     ("ring_skips_last_hop", "    for (r = 1; r < nshards; ++r) {\n        sc[1] = codes[r];",
      "    for (r = 1; r < nshards - 1; ++r) {\n        sc[1] = codes[r];"),
 ]
