@@ -21,7 +21,10 @@ The operations (see ``include/zq.h`` for the exact definitions):
                           hops, for comparison with the one-hop reduce;
   * ``quantize_interleaved`` / ``dequantize_interleaved``  Aquavit's metadata-
                           interleaved block records (scale, then codes);
-  * ``aquavit_schedule``  Aquavit's ascending width schedule -> (b, G).
+  * ``aquavit_schedule``  Aquavit's ascending width schedule -> (b, G);
+  * ``gemm_dequant``      y = x @ bf16(dequantize(W)).T on the tensor cores,
+                          the dequantization fused into the GEMM (AGoQ kernel
+                          fusion; the consumer of qwZ's gathered weights).
 """
 from __future__ import annotations
 
@@ -67,6 +70,8 @@ def _declare(L):
     L.zq_reduce_quantized_static.argtypes = [vp, vp, i32, i64, i32, i64, vp, vp, i32, i64, vp, vp]
     L.zq_reduce_quantized_static.restype = i32
     L.zq_fp8_accumulate.argtypes = [vp, vp, vp, i32, i64, i64, vp]
+    L.zq_gemm_dequant.argtypes = [vp, i64, i64, vp, vp, i32, i64, i64, vp, i32, vp]
+    L.zq_gemm_dequant.restype = i32
     L.zq_wait_selftest.argtypes = [i64, vp]
     L.zq_wait_selftest.restype = i32
     for f in ("zq_quantize", "zq_dequantize", "zq_reduce_quantized", "zq_fp8_accumulate"):
@@ -414,3 +419,25 @@ def wait_selftest(limit_us: int = 5000, stream=None):
     st = stream if stream is not None else torch.cuda.current_stream()
     _check(lib().zq_wait_selftest(int(limit_us), ctypes.c_void_p(st.cuda_stream)),
            "zq_wait_selftest")
+
+
+def gemm_dequant(x, w_codes, w_scales, fmt: int, G: int, N: int, out_dtype=None, out=None,
+                 stream=None):
+    """y = x @ W_hat.T with W_hat the bf16 dequantization of the N x K weight held
+    as (w_codes, w_scales) in (fmt, G) layout (zq_gemm_dequant). x: CUDA bf16
+    tensor M x K. Returns y (M x N, fp32 unless out_dtype / out say bf16)."""
+    torch = _torch()
+    _cuda_contig(x, "x")
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError("x must be a 2-D bf16 tensor")
+    M, K = x.shape
+    _need_pair(w_codes, w_scales, fmt, N * K, G, "weight")
+    if out is None:
+        out = torch.empty(M, N, dtype=out_dtype or torch.float32, device=x.device)
+    _cuda_contig(out, "out")
+    if out.numel() != M * N:
+        raise ValueError("out must hold M x N elements")
+    _check(lib().zq_gemm_dequant(x.data_ptr(), M, K, w_codes.data_ptr(), w_scales.data_ptr(), fmt,
+                                 G, N, out.data_ptr(), dtype_code(out.dtype), _stream(x, stream)),
+           "zq_gemm_dequant")
+    return out

@@ -20,8 +20,9 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libzq.so")
 
 UNITS = ["zq_api.cu", "zq_quantize.cu", "zq_dequantize.cu", "zq_reduce.cu", "zq_fp8.cu",
-         "zq_interleave.cu", "zq_reduce_few.cu"]
-HEADERS = ["zq_device.cuh", "zq_kernels.cuh", "zq_host.h"]
+         "zq_interleave.cu", "zq_reduce_few.cu", "zq_gemm.cu"]
+HEADERS = ["zq_device.cuh", "zq_kernels.cuh", "zq_host.h", "zq_reduce_launch.h", "zq_tc.cuh",
+           "zq_gemm.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # IEEE binary32 everywhere: no FMA contraction (fused forms are written

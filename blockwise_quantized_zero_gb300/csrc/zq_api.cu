@@ -199,7 +199,7 @@ zq_status zq_device_status(void *stream) {
     g_last_cuda_error = static_cast<int>(e);
     return ZQ_ERR_CUDA;
   }
-  const unsigned err = zq::take_reduce_device_error();
+  const unsigned err = zq::take_reduce_device_error() | zq::take_gemm_device_error();
   return (err & zq::kDevErrWaitTimeout) ? ZQ_ERR_TIMEOUT : ZQ_OK;
 }
 
@@ -577,6 +577,29 @@ zq_status zq_reduce_quantized_static(const void *const *codes, const float *cons
   a.one = 1.0f;
   return from_cuda(launch_reduce_static(codes, scales, a, format_in, format_out,
                                         as_stream(stream)));
+}
+
+zq_status zq_gemm_dequant(const void *x, int64_t M, int64_t K, const void *w_codes,
+                          const float *w_scales, int format, int64_t G, int64_t N, void *y,
+                          int y_dtype, void *stream) {
+  if (!bits_of(format) || (y_dtype != ZQ_F32 && y_dtype != ZQ_BF16)) return ZQ_ERR_UNSUPPORTED;
+  if (M < 0 || N < 0 || K < 0 || !valid_block(G)) return ZQ_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return ZQ_OK;
+  if (K == 0 || K % 64 != 0 || K % G != 0 || N % 64 != 0 || M > (int64_t(1) << 31) ||
+      N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+    return ZQ_ERR_INVALID_ARG;
+  if (((M + 127) / 128) * (N / 64) >= (int64_t(1) << 31)) return ZQ_ERR_INVALID_ARG;
+  if (!x || !w_codes || !w_scales || !y) return ZQ_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_codes) || !aligned16(w_scales) || !aligned16(y))
+    return ZQ_ERR_MISALIGNED;
+  const Range rx(x, size_t(M) * size_t(K) * 2u), rc(w_codes, zq_codes_bytes(format, N * K)),
+      rs(w_scales, size_t(zq_num_blocks(N * K, G)) * 4u),
+      ry(y, size_t(M) * size_t(N) * (y_dtype == ZQ_F32 ? 4u : 2u));
+  if (ry.overlaps(rx) || ry.overlaps(rc) || ry.overlaps(rs)) return ZQ_ERR_ALIAS;
+  for (const void *p : {x, w_codes, static_cast<const void *>(w_scales), static_cast<const void *>(y)})
+    if (zq_status st = check_device_ptr(p)) return st;
+  return from_cuda(launch_gemm_dequant(x, M, K, w_codes, w_scales, format, G, N, y, y_dtype,
+                                       as_stream(stream)));
 }
 
 zq_status zq_fp8_accumulate(void *main_codes, float *main_scales, const void *grad, int grad_dtype,

@@ -1,0 +1,437 @@
+// zq_gemm.cu -- launch unit of the dequant-fused GEMM (kernel design in
+// zq_gemm.cuh): y = x * bf16(dequantize(W))^T on the tcgen05 tensor cores.
+#include <cstring>
+#include <mutex>
+
+#include "zq_gemm.cuh"
+
+namespace zq {
+
+template <int FMT, int BN, int BM, int OUT>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_dequant_kernel(const __grid_constant__ CUtensorMap tm_x,
+                        const __grid_constant__ CUtensorMap tm_codes, const GemmArgs a) {
+  using GG = GemmGeom<FMT, BN, BM>;
+  constexpr int S = GG::kStages, NB = GG::kBRing, NACC = GG::kAccs, H = GG::kHalves;
+  constexpr int BITS = GG::kBits;
+  extern __shared__ uint8_t gemm_smem_raw[];
+  const uint32_t raw = smem_addr(gemm_smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-byte aligned (128-byte swizzle atoms)
+  uint8_t *gbase = gemm_smem_raw + (base - raw);
+  const uint32_t bar0 = base + GG::kBarOff;
+  // copy stage s: full (copies landed), empty (MMAs and dequantizers done with it)
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (S + s); };
+  // weight operand b: ready (dequantized), free (the MMAs that read it completed)
+  auto bready = [&](int b) { return bar0 + 8u * (2 * S + b); };
+  auto bfree = [&](int b) { return bar0 + 8u * (2 * S + NB + b); };
+  // accumulator c: full (last MMA of the tile completed), empty (read out)
+  auto acc_full = [&](int c) { return bar0 + 8u * (2 * S + 2 * NB + c); };
+  auto acc_empty = [&](int c) { return bar0 + 8u * (2 * S + 2 * NB + NACC + c); };
+  const uint32_t drain = bar0 + 8u * (2 * S + 2 * NB + 2 * NACC);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + GG::kBarOff + 8 * GG::kNumBars);
+  volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  auto sA = [&](int s) { return base + uint32_t(s) * GG::kStage; };
+  auto sC = [&](int s) { return base + uint32_t(s) * GG::kStage + GG::kABytes; };
+  auto sB = [&](int b) { return base + GG::kBOff + uint32_t(b) * GG::kBBytes; };
+  const uint8_t *gC0 = gbase + GG::kABytes;  // generic pointer to stage 0's codes
+
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntiles = a.tiles_m * a.tiles_n;
+  const int KB = int(a.K / kGemmBK);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1 + kGemmDequantWarps);
+    }
+    for (int b = 0; b < NB; ++b) {
+      mbar_init(bready(b), kGemmDequantWarps);
+      mbar_init(bfree(b), 1);
+    }
+    for (int c = 0; c < NACC; ++c) {
+      mbar_init(acc_full(c), 1);
+      mbar_init(acc_empty(c), kGemmEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort = 0;
+    mbar_init_fence();
+  }
+  if (w == 1) {
+    tc::tmem_alloc(smem_addr(tmem_slot), GG::kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (w == 0) {
+    // ---------------- producer: one lane issues the tiled copies ----------------
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&tm_x);
+      tc::tma_prefetch_desc(&tm_codes);
+      uint32_t u = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        int mb, nb;
+        gemm_tile(t, a.tiles_m, a.tiles_n, mb, nb);
+        for (int kb = 0; kb < KB; ++kb, ++u) {
+          const int s = int(u % S);
+          const uint32_t r = u / S;
+          if (r >= 1 && !gemm_wait_thread(empty(s), (r - 1) & 1u, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full(s), GG::kTxBytes);
+          tc::tma_load_2d(sA(s), &tm_x, kb * kGemmBK, mb * BM, full(s));
+          tc::tma_load_2d(sC(s), &tm_codes, kb * GG::kCodeRow, nb * BN, full(s));
+        }
+      }
+      if (!ok) {  // copies in flight land before the CTA's memory is released
+        const uint32_t first = u > uint32_t(S) ? u - S : 0u;
+        for (uint32_t v = first; v < u; ++v) (void)mbar_wait_thread(full(int(v % S)), (v / S) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (w == 1) {
+    // ---------------- MMA issuer: one lane ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kGemmMmaM, BN);
+      uint32_t u = 0;
+      int i = 0;
+      bool ok = true, issued = false;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++i) {
+        const int ab = i % NACC;
+        const uint32_t ra = uint32_t(i / NACC);
+        if (ra >= 1 && !gemm_wait_thread(acc_empty(ab), (ra - 1) & 1u, abort)) break;
+        tc::fence_after_sync();
+        const uint32_t d = tmem + uint32_t(ab * GG::kAccCols);
+        for (int kb = 0; kb < KB; ++kb, ++u) {
+          const int s = int(u % S), b = int(u % NB);
+          if (!gemm_wait_thread(full(s), (u / S) & 1u, abort) ||
+              !gemm_wait_thread(bready(b), (u / NB) & 1u, abort)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint64_t bd = tc::smem_desc_sw128(sB(b));
+#pragma unroll
+          for (int h = 0; h < H; ++h) {  // the 128-row halves share the weight operand
+            const uint64_t ad = tc::smem_desc_sw128(sA(s) + uint32_t(h * kGemmMmaM * 128));
+#pragma unroll
+            for (int k4 = 0; k4 < kGemmBK / 16; ++k4)  // +32 bytes along K per step
+              tc::mma_bf16(d + uint32_t(h * BN), ad + 2u * k4, bd + 2u * k4, idesc,
+                           (kb | k4) != 0 ? 1u : 0u);
+          }
+          tc::mma_commit(empty(s));
+          tc::mma_commit(bfree(b));
+          issued = true;
+        }
+        if (ok) tc::mma_commit(acc_full(ab));
+      }
+      if (issued) {  // every MMA has completed before the tensor memory is released
+        tc::mma_commit(drain);
+        (void)mbar_wait_thread(drain, 0u);
+      }
+    }
+    __syncwarp();
+  } else if (w < 2 + kGemmDequantWarps) {
+    // ---------------- dequantize: codes -> bf16 weight operand ----------------
+    // Thread dt owns the tasks i = 0 .. T-1: weight-tile row r0 + i * kRowStep
+    // (r0 = dt / 4), 16-code column c16 = dt % 4. Rows of one thread differ by
+    // a multiple of 8, so their swizzled chunk positions are the same and all
+    // shared-memory offsets are per-thread constants. The four threads of a
+    // row are adjacent lanes; the block scale of a row's 16-code run is loaded
+    // by one of them (c16 = 0, and c16 = 2 for G = 32, where a k-block holds
+    // two blocks), only when the k-block starts a new block (every G / 64
+    // k-blocks), one k-block ahead, and passed to the others by a shuffle.
+    constexpr int T = GG::kTasksPerThread;
+    constexpr int kRowStep = kGemmDqThreads / 4;
+    constexpr int CB = GG::kCodeRow;
+    const int dt = (w - 2) * 32 + lane, c16 = dt & 3, r0 = dt >> 2;
+    const uint32_t b_off0 = uint32_t(r0) * 128u + ((uint32_t(2 * c16) ^ uint32_t(r0 & 7)) << 4);
+    const uint32_t b_off1 = uint32_t(r0) * 128u + ((uint32_t(2 * c16 + 1) ^ uint32_t(r0 & 7)) << 4);
+    const int c_off = r0 * CB + c16 * (16 * BITS / 8);
+    const int lg = a.log2G;
+    const bool owner = lg == 5 ? (c16 & 1) == 0 : c16 == 0;
+    const int src = lg == 5 ? (lane & ~1) : (lane & ~3);
+    const int kpp = lg <= 6 ? 1 : 1 << (lg - 6);  // k-blocks per block
+    // Cursor one k-block ahead of the dequantization: tile f_t, k-block f_kb,
+    // each task's element index at k = 0.
+    int f_t = blockIdx.x, f_kb = 0;
+    int64_t f_e[T];
+    auto f_tile = [&]() {
+      if (f_t < ntiles) {
+        int mb, nb;
+        gemm_tile(f_t, a.tiles_m, a.tiles_n, mb, nb);
+#pragma unroll
+        for (int i = 0; i < T; ++i)
+          f_e[i] = (int64_t(nb) * BN + r0 + i * kRowStep) * a.K + c16 * 16;
+      }
+    };
+    auto f_next = [&]() {
+      if (++f_kb == KB) {
+        f_kb = 0;
+        f_t += gridDim.x;
+        f_tile();
+      }
+    };
+    float cur[T], nxt[T];
+    f_tile();
+#pragma unroll
+    for (int i = 0; i < T; ++i) {
+      cur[i] = 0.0f;
+      nxt[i] = 0.0f;
+      if (owner && dt + i * kGemmDqThreads < GG::kTasks) cur[i] = ld_nc_f32(a.scales + (f_e[i] >> lg));
+    }
+    f_next();
+    uint32_t u = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      for (int kb = 0; kb < KB; ++kb, ++u) {
+        const int s = int(u % S), b = int(u % NB);
+        const bool fresh = f_t < ntiles && f_kb % kpp == 0;  // the next k-block starts a block
+        if (fresh && owner) {
+#pragma unroll
+          for (int i = 0; i < T; ++i)
+            if (dt + i * kGemmDqThreads < GG::kTasks)
+              nxt[i] = ld_nc_f32(a.scales + ((f_e[i] + int64_t(f_kb) * kGemmBK) >> lg));
+        }
+        if (!gemm_wait_warp(full(s), (u / S) & 1u, abort) ||
+            (u >= uint32_t(NB) && !gemm_wait_warp(bfree(b), (u / NB - 1) & 1u, abort))) {
+          ok = false;
+          break;
+        }
+        const uint8_t *cs = gC0 + size_t(s) * GG::kStage + c_off;
+        const uint32_t bb = sB(b);
+#pragma unroll
+        for (int i = 0; i < T; ++i) {
+          const float sc = __shfl_sync(kFull, cur[i], src);
+          if (dt + i * kGemmDqThreads < GG::kTasks) {
+            uint32_t wv[Fmt<FMT>::kWords16];
+            load_codes16_smem<BITS>(cs + i * kRowStep * CB, wv);
+            float y[kVec];
+            dequant16<FMT>(wv, sc, y);
+            uint32_t p[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              __nv_bfloat162 h = __floats2bfloat162_rn(y[2 * q], y[2 * q + 1]);
+              p[q] = *reinterpret_cast<uint32_t *>(&h);
+            }
+            const uint32_t rb = bb + uint32_t(i * kRowStep * 128);
+            tc::st_shared_v4(rb + b_off0, p[0], p[1], p[2], p[3]);
+            tc::st_shared_v4(rb + b_off1, p[4], p[5], p[6], p[7]);
+          }
+        }
+        fence_proxy_async_smem();  // the tensor cores read these bytes through the async proxy
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bready(b));
+          mbar_arrive(empty(s));  // this warp is done with the stage's codes
+        }
+        if (fresh) {
+#pragma unroll
+          for (int i = 0; i < T; ++i) cur[i] = nxt[i];
+        }
+        f_next();
+      }
+    }
+  } else {
+    // ---------------- epilogue: tensor memory -> y ----------------
+    const int q = w & 3;  // this warp may read TMEM lanes [32q, 32q + 32)
+    int i = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+      int mb, nb;
+      gemm_tile(t, a.tiles_m, a.tiles_n, mb, nb);
+      const int ab = i % NACC;
+      if (!gemm_wait_warp(acc_full(ab), uint32_t(i / NACC) & 1u, abort)) break;
+      tc::fence_after_sync();
+#pragma unroll 1
+      for (int h = 0; h < H; ++h) {
+        const int64_t m = int64_t(mb) * BM + h * kGemmMmaM + q * 32 + lane;
+        const uint32_t taddr =
+            tmem + (uint32_t(q * 32) << 16) + uint32_t(ab * GG::kAccCols + h * BN);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          tc::tmem_ld32(taddr + uint32_t(c), v);
+          if (m < a.M) {
+            const int64_t off = m * a.N + int64_t(nb) * BN + c;
+            if constexpr (OUT == DT_F32) {
+              uint32_t *dst = static_cast<uint32_t *>(a.y) + off;
+#pragma unroll
+              for (int k = 0; k < 32; k += 4) st_v4(dst + k, v[k], v[k + 1], v[k + 2], v[k + 3]);
+            } else {
+              uint32_t hb[16];
+#pragma unroll
+              for (int k = 0; k < 16; ++k) {
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * k]),
+                                                          __uint_as_float(v[2 * k + 1]));
+                hb[k] = *reinterpret_cast<uint32_t *>(&b2);
+              }
+              uint16_t *dst = static_cast<uint16_t *>(a.y) + off;
+#pragma unroll
+              for (int k = 0; k < 16; k += 4) st_v4(dst + 2 * k, hb[k], hb[k + 1], hb[k + 2], hb[k + 3]);
+            }
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty(ab));
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (w == 1) tc::tmem_dealloc(tmem, GG::kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps (through the runtime's driver entry point, so the
+// library does not link the driver library), tile width, launch.
+// ---------------------------------------------------------------------------
+namespace {
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_tiled() {
+  static EncodeTiled fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      (void)cudaGetLastError();
+      p = nullptr;
+    }
+    return reinterpret_cast<EncodeTiled>(p);
+  }();
+  return fn;
+}
+
+// 2-D map of a row-major matrix of `rows` x `cols` elements (dtype, elem
+// bytes), row pitch `pitch` bytes, copied in boxes of box_rows x box_cols.
+cudaError_t make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t rows,
+                     uint64_t cols, uint64_t pitch, uint32_t box_rows, uint32_t box_cols,
+                     CUtensorMapSwizzle sw) {
+  EncodeTiled enc = encode_tiled();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {pitch};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int FMT, int BN, int BM, int OUT>
+cudaError_t go_gemm(const void *x, const void *codes, const GemmArgs &a, cudaStream_t st) {
+  using GG = GemmGeom<FMT, BN, BM>;
+  constexpr auto K = gemm_dequant_kernel<FMT, BN, BM, OUT>;
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, GG::kSmem);
+  if (attr != cudaSuccess) return attr;
+  CUtensorMap tx, tcd;
+  std::memset(&tx, 0, sizeof tx);
+  std::memset(&tcd, 0, sizeof tcd);
+  cudaError_t e = make_map(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, uint64_t(a.M), uint64_t(a.K),
+                           uint64_t(a.K) * 2u, BM, kGemmBK, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  const uint64_t code_pitch = uint64_t(a.K) * GG::kBits / 8u;
+  e = make_map(&tcd, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, uint64_t(a.N), code_pitch, code_pitch,
+               BN, GG::kCodeRow, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  const int tiles = a.tiles_m * a.tiles_n;
+  const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
+  K<<<grid, kGemmThreads, GG::kSmem, st>>>(tx, tcd, a);
+  return cudaGetLastError();
+}
+
+// The tile shapes built: 256 x 256 and 256 x 128 for problems with enough
+// rows, 128 x 128 and 128 x 64 otherwise.
+template <int FMT, int OUT>
+cudaError_t go_gemm_shape(const void *x, const void *codes, const GemmArgs &a, int bm, int bn,
+                          cudaStream_t st) {
+  if (bm == 256 && bn == 256) return go_gemm<FMT, 256, 256, OUT>(x, codes, a, st);
+  if (bm == 256 && bn == 128) return go_gemm<FMT, 128, 256, OUT>(x, codes, a, st);
+  if (bm == 128 && bn == 128) return go_gemm<FMT, 128, 128, OUT>(x, codes, a, st);
+  if (bm == 128 && bn == 64) return go_gemm<FMT, 64, 128, OUT>(x, codes, a, st);
+  return cudaErrorInvalidValue;
+}
+
+template <int OUT>
+cudaError_t go_gemm_fmt(const void *x, const void *codes, const GemmArgs &a, int fmt, int bm,
+                        int bn, cudaStream_t st) {
+  switch (fmt) {
+    case F_INT2: return go_gemm_shape<F_INT2, OUT>(x, codes, a, bm, bn, st);
+    case F_INT4: return go_gemm_shape<F_INT4, OUT>(x, codes, a, bm, bn, st);
+    case F_INT6: return go_gemm_shape<F_INT6, OUT>(x, codes, a, bm, bn, st);
+    case F_INT8: return go_gemm_shape<F_INT8, OUT>(x, codes, a, bm, bn, st);
+    case F_E4M3: return go_gemm_shape<F_E4M3, OUT>(x, codes, a, bm, bn, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+// Tile shape: the first of 256 x 256, 256 x 128, 128 x 128 whose column width
+// divides N and that still gives every SM an output tile (taller tiles share
+// one dequantized weight tile between more rows); 128 x 64 for small
+// problems. (128 x 256 would never come first: a problem it gives enough
+// tiles gives 256 x 128 as many.)
+void gemm_tile_shape(int64_t M, int64_t N, int &bm, int &bn) {
+  const int64_t sms = device_sm_count();
+  const int shapes[3][2] = {{256, 256}, {256, 128}, {128, 128}};
+  for (const auto &sh : shapes) {
+    const int64_t tm = (M + sh[0] - 1) / sh[0];
+    if (N % sh[1] == 0 && tm * (N / sh[1]) >= sms) {
+      bm = sh[0];
+      bn = sh[1];
+      return;
+    }
+  }
+  bm = 128;
+  bn = 64;
+}
+
+cudaError_t launch_gemm_dequant(const void *x, int64_t M, int64_t K, const void *codes,
+                                const float *scales, int fmt, int64_t G, int64_t N, void *y,
+                                int out_dt, cudaStream_t st) {
+  int bm = 128, bn = 64;
+  gemm_tile_shape(M, N, bm, bn);
+  GemmArgs a;
+  a.scales = scales;
+  a.y = y;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.log2G = log2_block(G);
+  a.tiles_m = int((M + bm - 1) / bm);
+  a.tiles_n = int(N / bn);
+  if (out_dt == DT_F32) return go_gemm_fmt<DT_F32>(x, codes, a, fmt, bm, bn, st);
+  if (out_dt == DT_BF16) return go_gemm_fmt<DT_BF16>(x, codes, a, fmt, bm, bn, st);
+  return cudaErrorInvalidValue;
+}
+
+unsigned take_gemm_device_error() {
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_dev_error, sizeof v) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  if (v != 0) {
+    const unsigned zero = 0;
+    (void)cudaMemcpyToSymbol(g_dev_error, &zero, sizeof zero);
+  }
+  return v;
+}
+
+}  // namespace zq

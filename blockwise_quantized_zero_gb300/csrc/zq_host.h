@@ -107,6 +107,13 @@ cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t st);
 unsigned take_reduce_device_error();
 unsigned take_reduce_few_device_error();
 
+// The dequant-fused GEMM (tcgen05): y = x * bf16(dequantize(codes, scales))^T.
+cudaError_t launch_gemm_dequant(const void *x, int64_t M, int64_t K, const void *codes,
+                                const float *scales, int fmt, int64_t G, int64_t N, void *y,
+                                int out_dt, cudaStream_t st);
+void gemm_tile_shape(int64_t M, int64_t N, int &bm, int &bn);
+unsigned take_gemm_device_error();
+
 cudaError_t launch_fp8_accumulate(void *codes, float *scales, const void *grad, int dt, int64_t n,
                                   int64_t G, cudaStream_t st, bool wide);
 

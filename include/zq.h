@@ -331,11 +331,41 @@ zq_status zq_fp8_accumulate(void *main_codes, float *main_scales, const void *gr
                             int64_t n, int64_t G, void *stream);
 
 /*
+ * zq_gemm_dequant -- the dequantization fused into the GEMM that consumes the
+ * quantized weights ([AGoQ] section "C. Kernel Fusion": quantization and
+ * dequantization fused with the adjacent GEMMs, their arithmetic on the CUDA
+ * cores and the GEMM on the tensor cores; [ZeRO++] qwZ: the layer computes
+ * with the dequantized gathered weights):
+ *     y[m][n] = sum over k of x[m][k] * W_hat[n][k],
+ *     W_hat[n][k] = bf16(fl32(q * s))  -- exactly zq_dequantize's bf16 output
+ *                                         for element n*K + k of W,
+ * accumulated in fp32 on the tensor cores (tcgen05, bf16 operands; the order
+ * of the fp32 additions is the hardware's), then stored as fp32 or rounded
+ * once to bf16. The bf16 weight matrix is never written to memory.
+ *   x          device, M x K bf16, row-major (K-major)
+ *   w_codes,   device, the zq_quantize output (format, G) of the N x K weight
+ *   w_scales   matrix flattened row-major: zq_codes_bytes(format, N*K) bytes
+ *              and zq_num_blocks(N*K, G) floats; G must divide K, so every
+ *              block lies within one row
+ *   y          device, M x N of y_dtype (ZQ_F32 or ZQ_BF16), row-major,
+ *              written in full; must not overlap x, w_codes or w_scales
+ *   M          >= 0 (any; rows past M in the last tile are not stored)
+ *   N, K       multiples of 64 (N, K, M <= 2^31)
+ * Errors: ZQ_ERR_UNSUPPORTED for an unknown format or y_dtype;
+ * ZQ_ERR_INVALID_ARG for sizes outside these rules; ZQ_ERR_MISALIGNED /
+ * ZQ_ERR_ALIAS as elsewhere. M = 0 or N = 0 enqueues nothing. The kernel's
+ * pipeline waits are bounded (zq_device_status reports one that ran out).
+ */
+zq_status zq_gemm_dequant(const void *x, int64_t M, int64_t K, const void *w_codes,
+                          const float *w_scales, int format, int64_t G, int64_t N, void *y,
+                          int y_dtype, void *stream);
+
+/*
  * zq_device_status -- errors the kernels found on the device. The reduce
- * kernels stream shard tiles into shared memory with bulk asynchronous copies
- * and wait for them with a time limit (2 s); a wait that runs out stops that
- * warp's work (its outputs are then incomplete) and sets a device error word
- * instead of hanging the GPU. This call waits for `stream` to finish
+ * kernels and the dequant-fused GEMM stream tiles into shared memory with
+ * bulk asynchronous copies and wait for them with a time limit (2 s); a wait
+ * that runs out stops that warp's work (its outputs are then incomplete) and
+ * sets a device error word instead of hanging the GPU. This call waits for `stream` to finish
  * (cudaStreamSynchronize), reads and clears the error words of all kernels,
  * and returns ZQ_ERR_TIMEOUT if any wait ran out since the last call,
  * ZQ_ERR_CUDA if the stream reported a CUDA error, and ZQ_OK otherwise.

@@ -230,3 +230,26 @@ def test_wait_selftest_limit_checked_before_the_device(L):
     refused before anything is enqueued (no device needed to see that)."""
     for bad in (0, -1, 100001, 1 << 40):
         assert L.zq_wait_selftest(bad, None) == INVALID
+
+
+def test_gemm_dequant_argument_errors(L):
+    """zq_gemm_dequant refuses bad formats, output types, shapes, alignment and
+    overlap before touching the device; empty problems enqueue nothing."""
+    x, c, s, y = BASE, BASE + (1 << 30), BASE + (2 << 30), BASE + (3 << 30)
+    g = L.zq_gemm_dequant
+    g.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,
+                  ctypes.c_void_p]
+    assert g(x, 128, 512, c, s, 3, 128, 256, y, O.F32, None) == UNSUPPORTED
+    assert g(x, 128, 512, c, s, O.INT8, 128, 256, y, O.F16, None) == UNSUPPORTED
+    assert g(x, 0, 512, c, s, O.INT8, 128, 256, y, O.F32, None) == OK
+    assert g(x, 128, 512, c, s, O.INT8, 128, 0, y, O.F32, None) == OK
+    assert g(x, 128, 500, c, s, O.INT8, 128, 256, y, O.F32, None) == INVALID   # K % 64
+    assert g(x, 128, 512, c, s, O.INT8, 128, 250, y, O.F32, None) == INVALID   # N % 64
+    assert g(x, 128, 64, c, s, O.INT8, 128, 256, y, O.F32, None) == INVALID    # G does not divide K
+    assert g(x, 128, 512, c, s, O.INT8, 48, 256, y, O.F32, None) == INVALID    # block size
+    assert g(x, -1, 512, c, s, O.INT8, 128, 256, y, O.F32, None) == INVALID
+    assert g(None, 128, 512, c, s, O.INT8, 128, 256, y, O.F32, None) == INVALID
+    assert g(x + 8, 128, 512, c, s, O.INT8, 128, 256, y, O.F32, None) == MISALIGNED
+    assert g(x, 128, 512, c, s, O.INT8, 128, 256, x + 4096, O.F32, None) == ALIAS
+    assert g(x, 128, 512, c, s, O.INT8, 128, 256, c + 64, O.BF16, None) == ALIAS

@@ -1,0 +1,125 @@
+"""The dequant-fused GEMM (zq_gemm_dequant, tcgen05 tensor cores) against the
+oracle, through the C ABI.
+
+Weights are quantized by the oracle (never by the GPU). Two kinds of check:
+
+* exact: small-integer activations and weights whose block scales are 1, so
+  every product and partial sum is an integer below 2^24 and the fp32 result
+  cannot depend on the order of the additions: the GPU must equal the integer
+  product exactly (fp32 output), or its single bf16 rounding (bf16 output);
+* bounded: random operands against the oracle's exact sum, within the error
+  bound of an fp32 accumulation of K/16 tensor-core steps in any order,
+  |y - exact| <= (K/16) 2^-22 sum_k |x w|, plus half a bf16 ulp of y
+  (2^-9 |y|, taken as 2^-8) for bf16 output.
+
+Shapes cover each output tile the launcher picks (256 x 256 with one
+accumulator, 256 x 128, 128 x 128 and 128 x 64 with two), several tiles per
+CTA (the stage ring and the accumulators wrap), a ragged last row tile, every
+code format and several block sizes.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+from helpers import bytes_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def zq():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import blockwise_quantized_zero_gb300 as zq
+
+    zq.lib()
+    return zq
+
+
+def _bf16_bits(x32):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(x32, np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+
+
+def _bf16_dev(bits, M, K):
+    import torch
+
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda().reshape(M, K)
+
+
+def _int_weights(r, N, K, G, fmt):
+    top = 448 if fmt == O.E4M3 else (1 << (O.BITS[fmt] - 1)) - 1
+    lim = 16 if fmt == O.E4M3 else top
+    W = r.integers(-lim, lim + 1, size=(N, K)).astype(np.int64)
+    W[:, ::G] = top * np.where(r.random((N, K // G)) < 0.5, -1, 1)  # block scale exactly 1
+    return W
+
+
+EXACT_CASES = [  # (M, N, K, fmt, G): tiles 256x256 / 128x128 / 128x64, ragged M, all formats
+    (4096 - 57, 2560, 1024, O.INT8, 128),
+    (1024, 2560, 512, O.INT4, 64),
+    (200, 1024, 768, O.INT2, 256),
+    (1024, 2560, 512, O.INT6, 32),
+    (1500, 1536, 1024, O.E4M3, 512),
+]
+
+
+@pytest.mark.parametrize("M,N,K,fmt,G", EXACT_CASES)
+def test_gemm_exact_small_integers(zq, M, N, K, fmt, G):
+    import torch
+
+    r = np.random.default_rng(M + N + K + fmt)
+    W = _int_weights(r, N, K, G, fmt)
+    X = r.integers(-16, 17, size=(M, K)).astype(np.int64)
+    codes, scales = O.quantize(W.astype(np.float32).ravel(), fmt, G)
+    assert np.all(scales == 1.0)
+    xd = _bf16_dev(_bf16_bits(X.astype(np.float32).ravel()), M, K)
+    want = X.astype(np.float64) @ W.astype(np.float64).T  # exact: integers below 2^53
+    assert np.abs(want).max() < 2 ** 24
+    y = zq.gemm_dequant(xd, bytes_dev(codes), bytes_dev(scales), fmt, G, N)
+    yb = zq.gemm_dequant(xd, bytes_dev(codes), bytes_dev(scales), fmt, G, N, out_dtype=torch.bfloat16)
+    zq.device_status()
+    got = to_host(y)
+    bad = np.argwhere(got != want.astype(np.float32))
+    assert bad.size == 0, f"{len(bad)} outputs differ, first at {bad[:4].tolist()}"
+    assert np.array_equal(to_host(yb), _bf16_bits(want.astype(np.float32).ravel()).reshape(M, N))
+
+
+BOUND_CASES = [  # tiles 256x128 / 128x64
+    (2048, 2560, 1024, O.INT8, 256),
+    (4096, 2560, 512, O.INT4, 32),
+    (768, 2560, 512, O.INT4, 128),
+    (128, 1024, 2048, O.INT4, 32),
+    (1000, 1536, 512, O.E4M3, 128),
+]
+
+
+@pytest.mark.parametrize("M,N,K,fmt,G", BOUND_CASES)
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_gemm_random_within_fp32_accumulation_bound(zq, M, N, K, fmt, G, out):
+    import torch
+
+    from blockwise_quantized_zero_gb300 import inputs
+
+    w32 = inputs.normal_f32(N * K, 0.02, 200 + fmt, stream=K)
+    codes, scales = O.quantize(w32, fmt, G)
+    xb = _bf16_bits(inputs.normal_f32(M * K, 1.0, 201, stream=M))
+    od = torch.float32 if out == "f32" else torch.bfloat16
+    y = to_host(zq.gemm_dequant(_bf16_dev(xb, M, K), bytes_dev(codes), bytes_dev(scales), fmt, G, N,
+                                out_dtype=od))
+    zq.device_status()
+    r = np.random.default_rng(7)
+    cnt = 4096
+    rows = np.concatenate([r.integers(0, M, cnt), np.full(N, M - 1), np.zeros(N, np.int64)])
+    cols = np.concatenate([r.integers(0, N, cnt), np.arange(N), np.arange(N)])
+    ref, mag = O.gemm_dequant(xb, M, K, codes, scales, fmt, G, N, rows=rows, cols=cols)
+    got = y[rows, cols].astype(np.float64) if out == "f32" else \
+        (y[rows, cols].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    tol = (K / 16) * 2.0 ** -22 * mag + (2.0 ** -8 * np.abs(ref) if out == "bf16" else 0.0)
+    err = np.abs(got - ref)
+    worst = float(np.max(err / np.maximum(tol, 1e-300)))
+    assert np.all(err <= tol), f"worst error {worst:.3f} of the bound"
