@@ -78,6 +78,17 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense bf16 tensor-core TFLOP/s: (burst, sustained, source)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:  # noqa: BLE001
+        return 1900.0, 1700.0, "fallback"
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
 
@@ -145,11 +156,11 @@ class Launch:
     """One timed unit: `fn` enqueues `kernels` launches of one kernel family
     that move `nbytes` algorithmic bytes in total."""
 
-    __slots__ = ("label", "family", "nbytes", "fn", "kernels")
+    __slots__ = ("label", "family", "nbytes", "fn", "kernels", "flops")
 
-    def __init__(self, label, family, nbytes, fn, kernels=1):
+    def __init__(self, label, family, nbytes, fn, kernels=1, flops=0):
         self.label, self.family, self.nbytes, self.fn = label, family, nbytes, fn
-        self.kernels = kernels
+        self.kernels, self.flops = kernels, flops
 
 
 class ForkedStreams:
@@ -332,7 +343,8 @@ class QwzFP16:
     def config(self):
         return {"workload": "qwz_fp16: one fp16 tensor of 1,048,576 elements N(0,0.02) with 0.1% "
                             "outliers x50 (seed 0), int8 G=256 quantize + dequantize->fp32; "
-                            "timed as CUDA graphs of 512 independent calls on 512 distinct copies",
+                            "timed as CUDA graphs of 512 independent calls on 512 distinct copies, "
+                            "and as one multi-tensor quantize call over the 512 copies",
                 "elements": self.n, "batched_copies": self.copies,
                 "graph_chains": self.streams,
                 "l2": "no flush: 512 distinct buffers per graph (1.6-2.7 GB per replay)",
@@ -382,6 +394,13 @@ class QwzFP16:
 
         capture(self.gq, lambda i: zq.quantize(self.src[i], zq.INT8, self.G, self.codes[i],
                                                self.scales[i]))
+        # the multi-tensor call (two launches of 256 tensors), captured so that
+        # its host-side argument checks are not timed as device time
+        zq.quantize_multi(self.src, zq.INT8, self.G, self.codes, self.scales)
+        torch.cuda.synchronize()
+        self.gm = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.gm, stream=s):
+            zq.quantize_multi(self.src, zq.INT8, self.G, self.codes, self.scales)
         capture(self.gd, lambda i: zq.dequantize(self.codes[i], self.scales[i], self.n, zq.INT8,
                                                  self.G, out=self.out[i]))
         torch.cuda.synchronize()
@@ -389,10 +408,13 @@ class QwzFP16:
     def launches(self):
         n, k = self.n, self.copies
         pb = packed_bytes(8, n, self.G)
+        zq = self.zq
         return [Launch(f"quantize fp16 int8 G=256 x{k} (graph)", "quantize", k * (2 * n + pb),
                        self.gq.replay, kernels=k),
                 Launch(f"dequantize int8 G=256 f32 x{k} (graph)", "dequantize", k * (pb + 4 * n),
-                       self.gd.replay, kernels=k)]
+                       self.gd.replay, kernels=k),
+                Launch(f"quantize fp16 int8 G=256 x{k} (one multi-tensor call, graph)",
+                       "quantize_multi", k * (2 * n + pb), self.gm.replay, kernels=(k + 255) // 256)]
 
     def setup_e2e(self):
         import torch
@@ -1002,6 +1024,140 @@ class Llama70B:
                              "G=32 round trips, single thread")
 
 
+class Llama70BGemm:
+    """The dequantization fused into the consumer GEMM: one Llama-3-70B
+    decoder layer's seven projections (N x K weights: q, o 8192 x 8192; k, v
+    1024 x 8192; gate, up 28672 x 8192; down 8192 x 28672, the layer's seeded
+    N(0, 0.02) bf16 matrices), held as int8 G=256 codes (qwZ's weight format),
+    applied to 4096 tokens of bf16 activations with zq_gemm_dequant, bf16
+    output. The bf16 weights are never materialized. For context the same
+    layer is also timed unfused (zq_dequantize to bf16, then cuBLAS bf16
+    matmul) during setup; that path is not part of the step."""
+
+    name = "llama70b_gemm"
+    dtype = "bf16 activations x int8 G=256 weights (dequantized to bf16 on chip), fp32 accumulate, bf16 out"
+    M = 4096
+    fmt, G = 8, 256
+
+    def config(self):
+        return {"workload": "llama70b_gemm: the seven projections of one Llama-3-70B decoder layer "
+                            "(855,638,016 weights, int8 G=256) on 4096 bf16 tokens, dequantization "
+                            "fused into the tcgen05 GEMM",
+                "tokens": self.M, "weights": 855638016,
+                "context_unfused_ms_per_step": getattr(self, "unfused_ms", None),
+                "context_cublas_bf16_ms_per_step": getattr(self, "cublas_ms", None),
+                "l2": "no flush: 0.9 GB of weights and 1.2 GB of activations/outputs per step"}
+
+    def setup(self):
+        import torch
+
+        import blockwise_quantized_zero_gb300 as zq
+        from blockwise_quantized_zero_gb300 import inputs
+
+        self.zq = zq
+        self.mats = []
+        for name, r, c, bits in inputs.llama70b_layer_bf16():
+            N, K = c, r  # output features x input features
+            w = _dev_bf16(bits)
+            codes, scales = zq.quantize(w, self.fmt, self.G)
+            self.mats.append((name, N, K, codes, scales))
+            del w, bits
+        self.x = {}
+        for K in sorted({K for _, _, K, _, _ in self.mats}):
+            self.x[K] = _dev_bf16(inputs.to_bf16_bits(inputs.normal_f32(self.M * K, 1.0, 7, stream=K))
+                                  ).reshape(self.M, K)
+        self.y = {name: torch.empty(self.M, N, dtype=torch.bfloat16, device="cuda")
+                  for name, N, _, _, _ in self.mats}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        self._context()
+
+    def _context(self):
+        """The unfused alternative on the same layer: dequantize to bf16, then
+        cuBLAS bf16 matmul (torch.matmul); and the matmul alone."""
+        import torch
+
+        zq = self.zq
+        wb = {name: torch.empty(N, K, dtype=torch.bfloat16, device="cuda")
+              for name, N, K, _, _ in self.mats}
+
+        def unfused():
+            for name, N, K, c, s in self.mats:
+                zq.dequantize(c, s, N * K, self.fmt, self.G, out=wb[name].view(-1))
+                torch.matmul(self.x[K], wb[name].t(), out=self.y[name])
+
+        def matmul_only():
+            for name, N, K, _, _ in self.mats:
+                torch.matmul(self.x[K], wb[name].t(), out=self.y[name])
+
+        out = []
+        for fn in (unfused, matmul_only):
+            for _ in range(2):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(5):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            out.append(round(e0.elapsed_time(e1) / 5, 3))
+        self.unfused_ms, self.cublas_ms = out
+        del wb
+        torch.cuda.empty_cache()
+
+    def launches(self):
+        zq, M = self.zq, self.M
+        out = []
+        for name, N, K, c, s in self.mats:
+            nb = 2 * M * K + packed_bytes(self.fmt, N * K, self.G) + 2 * M * N
+            out.append(Launch(f"gemm_dequant int8 G=256 {name} {M}x{N}x{K}", "gemm_dequant", nb,
+                              lambda name=name, N=N, K=K, c=c, s=s: zq.gemm_dequant(
+                                  self.x[K], c, s, self.fmt, self.G, N, out=self.y[name]),
+                              flops=2 * M * N * K))
+        return out
+
+    def setup_e2e(self):
+        """End to end: the q projection's activations from host memory, its
+        output back to host memory (weights stay resident, as gathered)."""
+        import torch
+
+        _, N, K, _, _ = self.mats[0]
+        self.h_x = self.x[K].cpu().pin_memory()
+        self.h_y = torch.empty(self.M, N, dtype=torch.bfloat16).pin_memory()
+        return 2 * self.M * K, 2 * self.M * N
+
+    def e2e_step(self):
+        name, N, K, c, s = self.mats[0]
+        self.x[K].copy_(self.h_x, non_blocking=True)
+        self.zq.gemm_dequant(self.x[K], c, s, self.fmt, self.G, N, out=self.y[name])
+        self.h_y.copy_(self.y[name], non_blocking=True)
+
+    def e2e_bytes(self):
+        _, N, K, _, _ = self.mats[0]
+        return 2 * self.M * K + packed_bytes(self.fmt, N * K, self.G) + 2 * self.M * N
+
+    def oracle_sample(self, sample=1 << 12):
+        """The oracle's exact dequant-fused products for `sample` output
+        elements of the q projection (K = 8192 products each)."""
+        import oracle as O
+        from blockwise_quantized_zero_gb300 import inputs
+
+        K = N = 8192
+        rows = 64
+        w = next(inputs.llama70b_layer_bf16(scale_rows=128))[3]  # 64 x 8192 of the q matrix
+        codes, scales = O.quantize(w, self.fmt, self.G, dtype=O.BF16)
+        x = inputs.to_bf16_bits(inputs.normal_f32(rows * K, 1.0, 7, stream=K))
+        r = np.random.default_rng(0)
+        rr, cc = r.integers(0, rows, sample), r.integers(0, rows, sample)
+
+        def run():
+            O.gemm_dequant(x, rows, K, codes, scales, self.fmt, self.G, rows, rows=rr, cols=cc)
+
+        nbytes = sample * (2 * K + K + 4 * K // self.G + 2)
+        return run, nbytes, (f"{sample:,} outputs of a {rows} x {rows} x {K} slice of the q "
+                             "projection, single thread")
+
+
 class AquavitSchedule:
     """Aquavit's weight codec over its ascending schedule: bpw(t) = 8 -
     6/(a + c t/T) with (a, c) = (0.9, 5) and T = 1000 steps, each step's width
@@ -1159,6 +1315,7 @@ class AquavitSchedule:
 
 WORKLOADS = {"gm_sweep": GMSweep, "qwz_fp16": QwzFP16, "qgz_reduce": QgzReduce,
              "agoq_fp8": AgoqFP8, "llama70b": Llama70B, "qgz_two_hop": QgzTwoHop,
+             "llama70b_gemm": Llama70BGemm,
              "aquavit_schedule": AquavitSchedule, "ring_study": RingStudy}
 
 
@@ -1334,8 +1491,9 @@ def time_cpu_all_cores(wl, sample):
 
 # The configurations timed after the headline workload in the same run (the
 # other single-GPU workloads of the method: the batched 1 Mi fp16 round trip,
-# the granularity sweep, the qgZ reduce and the AGoQ FP8 accumulate + reduce).
-EXTRA_CONFIGS = ("qwz_fp16", "gm_sweep", "qgz_reduce", "agoq_fp8")
+# the granularity sweep, the qgZ reduce and the AGoQ FP8 accumulate + reduce;
+# then the dequantization fused into the consumer GEMM).
+EXTRA_CONFIGS = ("qwz_fp16", "gm_sweep", "qgz_reduce", "agoq_fp8", "llama70b_gemm")
 EXTRA_STEPS = 20  # timed steps per extra configuration (at most --steps)
 NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, the ~8 TB/s nominal figure
 
@@ -1362,12 +1520,22 @@ def _groups(launches):
 
 
 def family_table(fam, peak):
-    return {k: {"gbs": round(v[1] / (v[0] / 1e3) / 1e9, 1),
-                "frac": round(v[1] / (v[0] / 1e3) / 1e9 / peak, 4),
-                "frac_of_nominal_hbm": round(v[1] / (v[0] / 1e3) / 1e9 / NOMINAL_HBM_GBS, 4),
-                "bytes_per_launch": int(v[1] / v[2]),
-                "us_per_launch": round(v[0] / v[2] * 1e3, 2), "launches": v[2]}
-            for k, v in fam.items()}
+    out = {}
+    burst, sustained, _ = measured_tensor_peak()
+    for k, v in fam.items():
+        row = {"gbs": round(v[1] / (v[0] / 1e3) / 1e9, 1),
+               "frac": round(v[1] / (v[0] / 1e3) / 1e9 / peak, 4),
+               "frac_of_nominal_hbm": round(v[1] / (v[0] / 1e3) / 1e9 / NOMINAL_HBM_GBS, 4),
+               "bytes_per_launch": int(v[1] / v[2]),
+               "us_per_launch": round(v[0] / v[2] * 1e3, 2), "launches": v[2]}
+        if v[3]:  # a contraction: its roofline is the tensor-core rate
+            tf = v[3] / (v[0] / 1e3) / 1e12
+            row.update({"tflops": round(tf, 1), "frac_of_bf16_burst": round(tf / burst, 4),
+                        "frac_of_bf16_sustained": round(tf / sustained, 4),
+                        "flops_per_launch": int(v[3] / v[2])})
+            row["bound"] = "tensor"
+        out[k] = row
+    return out
 
 
 def time_steps(launches, steps, world, stream, per_launch=True):
@@ -1417,10 +1585,11 @@ def time_steps(launches, steps, world, stream, per_launch=True):
     fam = {}
     for k in range(steps):
         for gi, (family, idx) in enumerate(groups):
-            f = fam.setdefault(family, [0.0, 0, 0])
+            f = fam.setdefault(family, [0.0, 0, 0, 0])
             f[0] += gevs[k][gi][0].elapsed_time(gevs[k][gi][1])
             f[1] += sum(launches[i].nbytes for i in idx)
             f[2] += sum(launches[i].kernels for i in idx)
+            f[3] += sum(launches[i].flops for i in idx)
     per_label = None
     if per_launch:
         per_label = {}
@@ -1500,9 +1669,26 @@ def run_gpu(args, rank, world, local):
 
     dominant = max(fam, key=lambda k: fam[k][0])
     peak, peak_src = measured_peak()
-    ms_sum, nbytes, count = fam[dominant]
+    ms_sum, nbytes, count, flops = fam[dominant]
     achieved = nbytes / (ms_sum / 1e3) / 1e9
     traffic = lookup_traffic(wl.name, dominant)
+    if flops:  # a contraction: the tensor-core roofline (burst: the family runs alone)
+        burst, _, tsrc = measured_tensor_peak()
+        tf = flops / (ms_sum / 1e3) / 1e12
+        roofline = {"bound": "tensor", "kernel": dominant, "achieved": round(tf, 1),
+                    "peak": burst, "peak_source": f"{tsrc} bf16_tflops (cuBLAS bf16 GEMM, burst)",
+                    "unit": "TFLOP/s", "frac": round(tf / burst, 4), "traffic": traffic,
+                    "algorithmic_flops_per_launch": int(flops / count),
+                    "us_per_launch": round(ms_sum / count * 1e3, 2)}
+    else:
+        roofline = {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1),
+                    "peak": peak, "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)",
+                    "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                    "frac_of_nominal_hbm": round(achieved / NOMINAL_HBM_GBS, 4),
+                    "nominal_hbm_gbs": NOMINAL_HBM_GBS,
+                    "target_uses": "frac (of the measured copy peak)",
+                    "algorithmic_bytes_per_launch": int(nbytes / count),
+                    "us_per_launch": round(ms_sum / count * 1e3, 2)}
     kpl = {l.label: l.kernels for l in launches}
     kernels = {k: {"gbs": round(v[1] / (v[0] / 1e3) / 1e9, 1),
                    "frac": round(v[1] / (v[0] / 1e3) / 1e9 / peak, 3),
@@ -1551,14 +1737,7 @@ def run_gpu(args, rank, world, local):
             "config": dict(main_config, parallelism=f"replicas x{world} (no collective)"),
             "frac_of_peak": round(value / peak, 4),
             "frac_of_nominal_hbm": round(value / NOMINAL_HBM_GBS, 4),
-            "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1),
-                         "peak": peak, "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)",
-                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                         "frac_of_nominal_hbm": round(achieved / NOMINAL_HBM_GBS, 4),
-                         "nominal_hbm_gbs": NOMINAL_HBM_GBS,
-                         "target_uses": "frac (of the measured copy peak)",
-                         "algorithmic_bytes_per_launch": int(nbytes / count),
-                         "us_per_launch": round(ms_sum / count * 1e3, 2)},
+            "roofline": roofline,
             "kernels": kernels,
             "cpu_baseline": cpu,
             "cpu_baseline_all_cores": cpu_all,

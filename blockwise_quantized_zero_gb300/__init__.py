@@ -72,6 +72,8 @@ def _declare(L):
     L.zq_fp8_accumulate.argtypes = [vp, vp, vp, i32, i64, i64, vp]
     L.zq_gemm_dequant.argtypes = [vp, i64, i64, vp, vp, i32, i64, i64, vp, i32, vp]
     L.zq_gemm_dequant.restype = i32
+    L.zq_quantize_multi.argtypes = [vp, vp, i32, i32, i32, i64, vp, vp, vp]
+    L.zq_quantize_multi.restype = i32
     L.zq_wait_selftest.argtypes = [i64, vp]
     L.zq_wait_selftest.restype = i32
     for f in ("zq_quantize", "zq_dequantize", "zq_reduce_quantized", "zq_fp8_accumulate"):
@@ -441,3 +443,34 @@ def gemm_dequant(x, w_codes, w_scales, fmt: int, G: int, N: int, out_dtype=None,
                                  G, N, out.data_ptr(), dtype_code(out.dtype), _stream(x, stream)),
            "zq_gemm_dequant")
     return out
+
+
+def quantize_multi(srcs, fmt: int, G: int, codes=None, scales=None, stream=None):
+    """zq_quantize of every tensor in `srcs` (same dtype) in one batched call
+    (zq_quantize_multi). Returns the lists (codes, scales); outputs are
+    allocated when not given."""
+    torch = _torch()
+    srcs = list(srcs)
+    if not srcs:
+        return [], []
+    dt = srcs[0].dtype
+    for t in srcs:
+        _cuda_contig(t, "src")
+        if t.dtype != dt:
+            raise ValueError("all tensors must have one dtype")
+    if codes is None:
+        codes = [empty_codes(fmt, t.numel(), t.device) for t in srcs]
+    if scales is None:
+        scales = [empty_scales(t.numel(), G, t.device) for t in srcs]
+    for t, c, s in zip(srcs, codes, scales):
+        _need_pair(c, s, fmt, t.numel(), G, "output")
+    k = len(srcs)
+
+    def arr(ts):
+        return (ctypes.c_void_p * k)(*[t.data_ptr() for t in ts])
+
+    sp, cp, kp = arr(srcs), arr(codes), arr(scales)
+    ns = (ctypes.c_int64 * k)(*[t.numel() for t in srcs])
+    _check(lib().zq_quantize_multi(sp, ns, k, dtype_code(dt), fmt, G, cp, kp,
+                                   _stream(srcs[0], stream)), "zq_quantize_multi")
+    return codes, scales

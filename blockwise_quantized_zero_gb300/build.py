@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libzq.so")
 
 UNITS = ["zq_api.cu", "zq_quantize.cu", "zq_dequantize.cu", "zq_reduce.cu", "zq_fp8.cu",
-         "zq_interleave.cu", "zq_reduce_few.cu", "zq_gemm.cu"]
+         "zq_interleave.cu", "zq_reduce_few.cu", "zq_gemm.cu", "zq_quantize_multi.cu"]
 HEADERS = ["zq_device.cuh", "zq_kernels.cuh", "zq_host.h", "zq_reduce_launch.h", "zq_tc.cuh",
            "zq_gemm.cuh"]
 

@@ -3,6 +3,7 @@
 // units. Every argument error is reported before any work is enqueued.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -85,6 +86,29 @@ zq_status check_device_ptr(const void *p) {
     return ZQ_ERR_INVALID_ARG;
   }
   return ZQ_OK;
+}
+
+// True when some output range overlaps another range (input or output);
+// inputs may overlap each other. Sort and sweep: O(n log n).
+bool any_output_overlap(std::vector<Range> ins, std::vector<Range> outs) {
+  struct Tagged {
+    uintptr_t lo, hi;
+    bool out;
+  };
+  std::vector<Tagged> all;
+  all.reserve(ins.size() + outs.size());
+  for (const Range &r : ins)
+    if (r.lo != r.hi) all.push_back({r.lo, r.hi, false});
+  for (const Range &r : outs)
+    if (r.lo != r.hi) all.push_back({r.lo, r.hi, true});
+  std::sort(all.begin(), all.end(), [](const Tagged &x, const Tagged &y) { return x.lo < y.lo; });
+  uintptr_t end_all = 0, end_out = 0;
+  for (const Tagged &r : all) {
+    if (r.lo < (r.out ? end_all : end_out)) return true;
+    end_all = std::max(end_all, r.hi);
+    if (r.out) end_out = std::max(end_out, r.hi);
+  }
+  return false;
 }
 
 zq_status from_cuda(cudaError_t e) {
@@ -219,6 +243,59 @@ zq_status zq_quantize(const void *src, int src_dtype, int64_t n, int format, int
   const bool wide = aligned32(src);
   return from_cuda(launch_quantize(src, src_dtype, n, format, G, codes, scales, as_stream(stream),
                                    wide));
+}
+
+zq_status zq_quantize_multi(const void *const *src, const int64_t *n, int count, int src_dtype,
+                            int format, int64_t G, void *const *codes, float *const *scales,
+                            void *stream) {
+  if (!bits_of(format) || !elem_bytes(src_dtype)) return ZQ_ERR_UNSUPPORTED;
+  if (count < 0 || !valid_block(G)) return ZQ_ERR_INVALID_ARG;
+  if (count == 0) return ZQ_OK;
+  if (!src || !n || !codes || !scales) return ZQ_ERR_INVALID_ARG;
+  std::vector<Range> ins, outs;
+  bool wide = true;
+  for (int k = 0; k < count; ++k) {
+    if (n[k] < 0) return ZQ_ERR_INVALID_ARG;
+    if (n[k] == 0) continue;
+    if (!src[k] || !codes[k] || !scales[k]) return ZQ_ERR_INVALID_ARG;
+    if (!aligned16(src[k]) || !aligned16(codes[k]) || !aligned16(scales[k])) return ZQ_ERR_MISALIGNED;
+    if (!aligned32(src[k])) wide = false;
+    ins.emplace_back(src[k], size_t(n[k]) * elem_bytes(src_dtype));
+    outs.emplace_back(codes[k], zq_codes_bytes(format, n[k]));
+    outs.emplace_back(scales[k], size_t(zq_num_blocks(n[k], G)) * 4u);
+  }
+  if (any_output_overlap(std::move(ins), std::move(outs))) return ZQ_ERR_ALIAS;
+  for (int k = 0; k < count; ++k) {
+    if (n[k] == 0) continue;
+    for (const void *p : {src[k], static_cast<const void *>(codes[k]),
+                          static_cast<const void *>(scales[k])})
+      if (zq_status st = check_device_ptr(p)) return st;
+  }
+  // launches of up to kMultiMax tensors (empty tensors are left out)
+  MultiArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.wide = wide ? 1 : 0;
+  int m = 0;
+  auto flush = [&]() -> zq_status {
+    if (m == 0) return ZQ_OK;
+    a.count = m;
+    const zq_status st = from_cuda(launch_quantize_multi(a, src_dtype, format, G, as_stream(stream)));
+    m = 0;
+    a.tile0[0] = 0;
+    return st;
+  };
+  a.tile0[0] = 0;
+  for (int k = 0; k < count; ++k) {
+    if (n[k] == 0) continue;
+    a.src[m] = src[k];
+    a.codes[m] = static_cast<uint8_t *>(codes[k]);
+    a.scales[m] = scales[k];
+    a.n[m] = n[k];
+    a.tile0[m + 1] = a.tile0[m] + n[k] / kTile;
+    if (++m == kMultiMax)
+      if (zq_status st = flush()) return st;
+  }
+  return flush();
 }
 
 zq_status zq_quantize_reordered(const void *src, int src_dtype, int64_t n, int format, int64_t G,

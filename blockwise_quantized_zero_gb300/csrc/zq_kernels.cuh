@@ -319,6 +319,118 @@ __global__ void __launch_bounds__(kThreads, 3) quantize_kernel(const void *__res
   if (c.owns_tail(n)) quantize_tail<DT, FMT, G, IL>(src, codes, scales, nfull * kTile, n, c.lane);
 }
 
+// ---------------------------------------------------------------------------
+// Multi-tensor quantize: one launch over a list of tensors (same element
+// type, format and block size). The full tiles of all tensors are numbered
+// consecutively (tensor k owns tiles [tile0[k], tile0[k+1])) and walked in
+// the same grid-stride order as one large tensor, so the warps stream one
+// narrow window of memory at a time. A queued fix-up run also records its
+// tensor, so the queue is flushed in full batches as in quantize_kernel.
+// Each tensor's partial last tile goes to warp k % nwarps.
+// ---------------------------------------------------------------------------
+constexpr int kMultiMax = 256;  // tensors per launch (the list travels in the kernel parameters)
+
+struct MultiArgs {
+  const void *src[kMultiMax];
+  uint8_t *codes[kMultiMax];
+  float *scales[kMultiMax];
+  int64_t n[kMultiMax];
+  int64_t tile0[kMultiMax + 1];  // prefix sums of full tiles
+  int count;
+  int wide;
+};
+
+// Fix the queued runs [first, first + count) of warp w, each in its own
+// tensor (quantize_flush with per-entry source and code pointers).
+template <int DT, int FMT, int G>
+__device__ __noinline__ void quantize_flush_multi(FixQueue<DT> &fq, const int16_t (&fk)[kQueue],
+                                                  int w, int first, int count, const MultiArgs &a,
+                                                  int lane, bool wide) {
+  constexpr int B = Fmt<FMT>::kBits, W = Fmt<FMT>::kWords16;
+  __syncwarp();
+  for (int base = 0; base < count; base += 32) {
+    const int i = base + lane;
+    if (i < count) {
+      const int slot = first + i;
+      const int64_t e = fq.e[w][slot];
+      const float s = fq.s[w][slot];
+      const int k = fk[slot];
+      uint32_t raw[kRawWords<DT>];
+      if constexpr (kStash<DT>) {
+#pragma unroll
+        for (int q = 0; q < kRawWords<DT>; ++q) raw[q] = fq.raw[w][slot][q];
+      } else {
+        load16_raw<DT>(a.src[k], e, raw, wide);
+      }
+      float x[kVec];
+      widen16<DT>(raw, x);
+      const float r = safe_rcp(s);
+      uint8_t *cp = a.codes[k] + code_off<false, B>(e, log2_of(G));
+      uint32_t wd[W];
+      const bool normal = (FMT == F_E4M3) ? scale_is_normal(s) : (s == 0.0f || scale_is_normal(s));
+      if (normal && FMT != F_E4M3) {
+        quant16_fix<FMT>(x, s, r, 1u, wd);
+      } else if (normal) {
+        ld_v4(cp, wd[0], wd[1], wd[2], wd[3]);
+        quant16_fix<FMT>(x, s, r, 1u, wd);
+      } else {
+        quant16_exact<FMT>(x, s, wd);
+      }
+      put_codes16<false, B>(cp, wd);
+    }
+  }
+  __syncwarp();
+}
+
+template <int DT, int FMT, int G>
+__global__ void __launch_bounds__(kThreads, 3) quantize_multi_kernel(const __grid_constant__ MultiArgs a) {
+  const WarpCursor c;
+  const bool wd = a.wide != 0;
+  const int64_t total = a.tile0[a.count];
+  __shared__ FixQueue<DT> fq;
+  __shared__ int16_t fqk[kWarps][kQueue];  // tensor of each queued run
+  const int w = threadIdx.x >> 5;
+  int count = 0;  // warp-uniform
+  uint32_t raw[kU][kRawWords<DT>];
+  int k = 0, kn = 0;  // tensors of the current and the next tile (they only grow)
+  auto load_tile = [&](int64_t t, int kk) {
+    const int64_t e0 = (t - a.tile0[kk]) * kTile;
+#pragma unroll
+    for (int j = 0; j < kU; ++j) load16_raw<DT>(a.src[kk], e0 + j * kRun + c.lane * kVec, raw[j], wd);
+  };
+  if (c.warp < total) {
+    while (c.warp >= a.tile0[kn + 1]) ++kn;
+    load_tile(c.warp, kn);
+  }
+  for (int64_t t = c.warp; t < total; t += c.nwarps) {
+    uint32_t cur[kU][kRawWords<DT>];
+#pragma unroll
+    for (int j = 0; j < kU; ++j)
+#pragma unroll
+      for (int q = 0; q < kRawWords<DT>; ++q) cur[j][q] = raw[j][q];
+    k = kn;
+    const int64_t tn = t + c.nwarps;
+    if (tn < total) {
+      while (tn >= a.tile0[kn + 1]) ++kn;
+      load_tile(tn, kn);
+    }
+    const int c0 = count;
+    quantize_tile<DT, FMT, G, false>(cur, a.codes[k], a.scales[k], (t - a.tile0[k]) * kTile,
+                                     c.lane, fq, w, count);
+    for (int i = c0 + c.lane; i < count; i += 32) fqk[w][i] = int16_t(k);
+    while (count >= 32) {  // fix full batches right away, newest first
+      count -= 32;
+      quantize_flush_multi<DT, FMT, G>(fq, fqk[w], w, count, 32, a, c.lane, wd);
+    }
+  }
+  if (count) quantize_flush_multi<DT, FMT, G>(fq, fqk[w], w, 0, count, a, c.lane, wd);
+  for (int kk = int(c.warp); kk < a.count; kk += int(c.nwarps)) {
+    if (a.n[kk] % kTile)
+      quantize_tail<DT, FMT, G, false>(a.src[kk], a.codes[kk], a.scales[kk],
+                                       (a.n[kk] / kTile) * kTile, a.n[kk], c.lane);
+  }
+}
+
 // ===========================================================================
 // Dequantize
 // ===========================================================================

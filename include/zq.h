@@ -123,6 +123,26 @@ zq_status zq_quantize(const void *src, int src_dtype, int64_t n, int format, int
                       float *scales, void *stream);
 
 /*
+ * zq_quantize_multi -- zq_quantize of `count` tensors in as few launches as
+ * possible (one per 256 tensors): the results are exactly those of `count`
+ * separate zq_quantize calls, but a list of small tensors (a layer's weights,
+ * many buffers of a few MB each) streams at the rate of one large tensor
+ * instead of paying a launch and a partly filled grid per tensor. A library
+ * entry point with no counterpart on the pages; the tensor list is copied into
+ * the kernel parameters, so nothing is allocated.
+ *   src, n, codes, scales  HOST arrays of `count` entries: tensor k has n[k]
+ *             elements at src[k] (device) and writes codes[k], scales[k]
+ *             (device) as zq_quantize(src[k], ..., n[k], ...) would; n[k] = 0
+ *             is allowed (its pointers are then ignored)
+ *   src_dtype, format, G   shared by all tensors
+ * Errors as zq_quantize, checked for every tensor before anything is
+ * enqueued; no output may overlap any input or any other output.
+ */
+zq_status zq_quantize_multi(const void *const *src, const int64_t *n, int count, int src_dtype,
+                            int format, int64_t G, void *const *codes, float *const *scales,
+                            void *stream);
+
+/*
  * zq_dequantize -- inverse of zq_quantize ([ZeRO++] qwZ: dequantize after the
  * gather; qgZ: dequantize before the full-precision reduction).
  *   codes, scales  device, as written by zq_quantize(format, G)

@@ -253,3 +253,30 @@ def test_gemm_dequant_argument_errors(L):
     assert g(x + 8, 128, 512, c, s, O.INT8, 128, 256, y, O.F32, None) == MISALIGNED
     assert g(x, 128, 512, c, s, O.INT8, 128, 256, x + 4096, O.F32, None) == ALIAS
     assert g(x, 128, 512, c, s, O.INT8, 128, 256, c + 64, O.BF16, None) == ALIAS
+
+
+def test_quantize_multi_argument_errors(L):
+    """zq_quantize_multi: bad format / type, negative counts and sizes, null,
+    misaligned and overlapping buffers are refused before any work."""
+    def call(srcs, ns, codes, scales, fmt=O.INT8, dt=O.F16, G=256, count=None):
+        k = len(srcs) if count is None else count
+        arr = lambda xs: (ctypes.c_void_p * max(1, len(xs)))(*xs)  # noqa: E731
+        return L.zq_quantize_multi(arr(srcs), (ctypes.c_int64 * max(1, len(ns)))(*ns), k, dt, fmt, G,
+                                   arr(codes), arr(scales), None)
+
+    s0, s1 = BASE, BASE + (1 << 24)
+    c0, c1 = BASE + (2 << 24), BASE + (3 << 24)
+    k0, k1 = BASE + (4 << 24), BASE + (5 << 24)
+    assert call([s0], [1024], [c0], [k0], fmt=3) == UNSUPPORTED
+    assert call([s0], [1024], [c0], [k0], dt=7) == UNSUPPORTED
+    assert call([s0], [1024], [c0], [k0], count=-1) == INVALID
+    assert call([s0], [1024], [c0], [k0], count=0) == OK
+    assert call([s0], [1024], [c0], [k0], G=100) == INVALID
+    assert call([s0, s1], [1024, -5], [c0, c1], [k0, k1]) == INVALID
+    assert call([s0, None], [1024, 8], [c0, c1], [k0, k1]) == INVALID
+    assert call([s0, 0], [1024, 0], [c0, 0], [k0, 0]) != MISALIGNED  # empty tensors: pointers ignored
+    assert call([s0, s1 + 8], [1024, 1024], [c0, c1], [k0, k1]) == MISALIGNED
+    assert call([s0, s1], [1024, 1024], [c0, c0 + 512], [k0, k1]) == ALIAS   # outputs overlap
+    assert call([s0, s1], [1024, 1024], [c0, s0], [k0, k1]) == ALIAS         # output on an input
+    assert call([s0, s1], [1024, 1024], [c0, c1], [k0, c1 + 128]) == ALIAS   # scales on codes
+    assert call([s0, s0], [1024, 1024], [c0, c1], [k0, k1]) != ALIAS         # shared input is fine

@@ -123,3 +123,64 @@ def test_gemm_random_within_fp32_accumulation_bound(zq, M, N, K, fmt, G, out):
     err = np.abs(got - ref)
     worst = float(np.max(err / np.maximum(tol, 1e-300)))
     assert np.all(err <= tol), f"worst error {worst:.3f} of the bound"
+
+
+@pytest.mark.parametrize("M,N,K,fmt,G", [(1, 64, 64, O.INT8, 64), (1, 128, 64, O.INT4, 32),
+                                         (129, 192, 128, O.INT6, 128), (300, 64, 1024, O.INT2, 1024)])
+def test_gemm_edge_shapes_exact(zq, M, N, K, fmt, G):
+    """One row, the smallest N and K (one k-block), a row tile of one row."""
+    r = np.random.default_rng(M * 7 + N + K)
+    W = _int_weights(r, N, K, G, fmt)
+    X = r.integers(-16, 17, size=(M, K)).astype(np.int64)
+    codes, scales = O.quantize(W.astype(np.float32).ravel(), fmt, G)
+    y = zq.gemm_dequant(_bf16_dev(_bf16_bits(X.astype(np.float32).ravel()), M, K), bytes_dev(codes),
+                        bytes_dev(scales), fmt, G, N)
+    zq.device_status()
+    assert np.array_equal(to_host(y), (X.astype(np.float64) @ W.astype(np.float64).T).astype(np.float32))
+
+
+def test_gemm_empty_problem_enqueues_nothing(zq):
+    import torch
+
+    codes = torch.zeros(64 * 64, dtype=torch.uint8, device="cuda")
+    scales = torch.zeros(64 * 64 // 32, dtype=torch.float32, device="cuda")
+    x = torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda")
+    assert zq.gemm_dequant(x, codes, scales, O.INT8, 32, 64).shape == (0, 64)
+    zq.device_status()
+
+
+def test_gemm_llama70b_layer_sampled(zq):
+    """The benchmark configuration: the seven Llama-3-70B layer projections
+    applied to 4096 tokens of bf16 activations. Each seeded bf16 matrix of the
+    layer (listed input x output features) is read as the N x K weight of the
+    projection (N = its output features, K = its input features; the same
+    N(0, 0.02) bytes), quantized int8 G=256 by the oracle. 4096 sampled
+    outputs of each projection, plus a whole output row and column, against
+    the oracle within the fp32 accumulation bound (bf16 output)."""
+    import torch
+
+    import fullsize as F
+    from blockwise_quantized_zero_gb300 import inputs
+
+    M, fmt, G = 4096, O.INT8, 256
+    xs = {}
+    r = np.random.default_rng(11)
+    for name, rows, cols, bits in inputs.llama70b_layer_bf16():
+        N, K = cols, rows  # output features x input features
+        codes, scales = F.oracle_quantize_full(bits, fmt, G, dtype=O.BF16)
+        if K not in xs:
+            xs[K] = _bf16_bits(inputs.normal_f32(M * K, 1.0, 300, stream=K))
+        xb = xs[K]
+        y = to_host(zq.gemm_dequant(_bf16_dev(xb, M, K), bytes_dev(codes), bytes_dev(scales), fmt, G,
+                                    N, out_dtype=torch.bfloat16))
+        zq.device_status()
+        mrow, ncol = int(r.integers(0, M)), int(r.integers(0, N))
+        rows_ = np.concatenate([r.integers(0, M, 4096), np.full(N, mrow), np.arange(M)])
+        cols_ = np.concatenate([r.integers(0, N, 4096), np.arange(N), np.full(M, ncol)])
+        ref, mag = O.gemm_dequant(xb, M, K, codes, scales, fmt, G, N, rows=rows_, cols=cols_)
+        got = (y[rows_, cols_].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        tol = (K / 16) * 2.0 ** -22 * mag + 2.0 ** -8 * np.abs(ref)
+        err = np.abs(got - ref)
+        assert np.all(err <= tol), (name, float(np.max(err / tol)))
+        del codes, scales, y
+    torch.cuda.empty_cache()

@@ -366,3 +366,20 @@ def test_round_trip_through_the_gpu_only(zq):
         y = zq.dequantize(c, s, x.size, fmt, 256, out_dtype=torch.bfloat16)
         wc, ws = O.quantize(x, fmt, 256, dtype=O.BF16)
         assert_same_bits(to_host(y), O.dequantize(wc, ws, x.size, fmt, 256, O.BF16), fid(fmt))
+
+
+@pytest.mark.parametrize("fmt", [O.INT8, O.INT4, O.E4M3])
+def test_quantize_every_finite_fp16_value(zq, fmt):
+    """Every finite binary16 bit pattern (subnormals, zeros of both signs,
+    the largest values) as quantize input: blocks of 32 consecutive patterns,
+    so each block's scale and every code depend on the exact widening."""
+    import torch
+
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    finite = bits[(bits & 0x7C00) != 0x7C00].astype(np.uint16)
+    n = finite.size - finite.size % 32
+    x = finite[:n].view(np.float16)
+    c, s = zq.quantize(torch.from_numpy(x.copy()).cuda(), fmt, 32)
+    wc, ws = O.quantize(x, fmt, 32)
+    assert np.array_equal(to_host(c), wc)
+    assert np.array_equal(as_bits(to_host(s)), as_bits(ws))
