@@ -1755,6 +1755,18 @@ def run_gpu(args, rank, world, local):
     return line
 
 
+# The DRAM bytes per launch in profiles/ncu_traffic.json were captured on
+# particular kernel sources: the fused GEMM's family on all of csrc/, the
+# codec families (quantize, dequantize, reduce, FP8 accumulate and their
+# variants) on csrc/ without the GEMM's own files. A capture whose source set
+# has changed since is not reported.
+GEMM_ONLY_SOURCES = ("zq_gemm.cu", "zq_gemm.cuh", "zq_tc.cuh")
+
+
+def source_set(family: str) -> str:
+    return "gemm" if family.startswith("gemm") else "codec"
+
+
 def lookup_traffic(workload: str, family: str):
     """DRAM bytes per launch of a workload's kernel family from the committed
     ncu summaries, if they were taken on the current kernel sources; None
@@ -1765,17 +1777,22 @@ def lookup_traffic(workload: str, family: str):
             d = json.load(f)
     except Exception:  # noqa: BLE001
         return None
-    if d.get("csrc_sha") != csrc_sha():
+    sset = source_set(family)
+    if d.get("source_sets", {}).get(sset) != csrc_sha(sset):
         return None
     return d.get("workloads", {}).get(workload, {}).get(family)
 
 
-def csrc_sha() -> str:
+def csrc_sha(sset: str = "gemm") -> str:
+    """Hash of the kernel sources of a source set ("gemm": all of csrc/;
+    "codec": csrc/ without the GEMM's own files)."""
     import hashlib
 
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "blockwise_quantized_zero_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
+        if sset == "codec" and name in GEMM_ONLY_SOURCES:
+            continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]

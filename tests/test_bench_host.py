@@ -22,11 +22,20 @@ def test_packed_bytes_match_the_oracle(fmt):
 
 
 def test_traffic_is_keyed_by_the_kernel_sources(monkeypatch):
-    with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
-        d = json.load(f)
-    wl, fam = "gm_sweep", "quantize"
-    monkeypatch.setattr(bench, "csrc_sha", lambda: d["csrc_sha"])
-    assert bench.lookup_traffic(wl, fam) == d["workloads"][wl][fam]
-    monkeypatch.setattr(bench, "csrc_sha", lambda: "0" * 16)
-    assert bench.lookup_traffic(wl, fam) is None
+    d = {"source_sets": {"codec": "c" * 16, "gemm": "g" * 16},
+         "workloads": {"llama70b": {"quantize": 123}, "llama70b_gemm": {"gemm_dequant": 456}}}
+    monkeypatch.setattr(bench.json, "load", lambda f: d)
+    monkeypatch.setattr(bench, "csrc_sha", lambda sset: {"codec": "c" * 16, "gemm": "g" * 16}[sset])
+    assert bench.lookup_traffic("llama70b", "quantize") == 123
+    assert bench.lookup_traffic("llama70b_gemm", "gemm_dequant") == 456
+    # a change in the GEMM's sources leaves the codec captures valid, and the reverse
+    monkeypatch.setattr(bench, "csrc_sha", lambda sset: {"codec": "c" * 16, "gemm": "x" * 16}[sset])
+    assert bench.lookup_traffic("llama70b", "quantize") == 123
+    assert bench.lookup_traffic("llama70b_gemm", "gemm_dequant") is None
+    monkeypatch.setattr(bench, "csrc_sha", lambda sset: "0" * 16)
+    assert bench.lookup_traffic("llama70b", "quantize") is None
 
+
+def test_source_sets_split_the_gemm_files():
+    assert bench.source_set("gemm_dequant") == "gemm" and bench.source_set("quantize") == "codec"
+    assert bench.csrc_sha("codec") != bench.csrc_sha("gemm")
