@@ -10,8 +10,11 @@ of the other configurations (``--configs``, reported under ``configs``):
 qwz_fp16 (1 Mi fp16 weights with outliers, int8 G=256, batched over 512
 tensors), gm_sweep (8192x8192 bf16, b in {2,4,6,8} x G in {1024..32}),
 qgz_reduce (8 int4 shards of 134,217,728 gradients -> int4 G=128 and int8
-G=256) and agoq_fp8 (E4M3 main gradient of 268,435,456 elements, 4 accumulate
-steps + 8-shard FP8 reduce). Further workloads (``--workload``): qgz_two_hop
+G=256), agoq_fp8 (E4M3 main gradient of 268,435,456 elements, 4 accumulate
+steps + 8-shard FP8 reduce), llama70b_batched (the headline layer through one
+multi-tensor quantize and one multi-tensor dequantize call per scheme) and
+llama70b_gemm (the layer's projections on 4096 tokens with the dequantization
+fused into the tensor-core GEMM). Further workloads (``--workload``): qgz_two_hop
 (qgZ's reordered quantize and two-hop reduce, 2 nodes x 4 GPUs simulated),
 aquavit_schedule (the 1000-step ascending width schedule, in the metadata-
 interleaved and the planar layout) and ring_study (the ring reduce-scatter's
@@ -906,18 +909,23 @@ class AgoqFP8:
 class Llama70B:
     """One Llama-3-70B decoder layer's bf16 weights (7 matrices, 855,638,016
     elements, N(0, 0.02), seed 5): int8 G=256 and 6-bit G=32 quantize +
-    dequantize -> bf16, one call per matrix."""
+    dequantize -> bf16, one call per matrix (`llama70b_batched`: per scheme one
+    zq_quantize_multi and one zq_dequantize_multi call over the seven matrices,
+    with the same results)."""
 
     name = "llama70b"
     dtype = "bf16 in, int8 / int6 codes + fp32 scales, bf16 out (fp32 arithmetic)"
     schemes = ((8, 256), (6, 32))
+    batched = False
 
     def config(self):
+        how = ("per scheme one multi-tensor quantize and one multi-tensor dequantize call over the "
+               "seven matrices" if self.batched else "one call per matrix")
         return {"workload": "llama70b: one Llama-3-70B decoder layer in bf16 (q,o 8192x8192; k,v "
                             "8192x1024; gate,up 8192x28672; down 28672x8192; 855,638,016 elements, "
                             "N(0,0.02)), quantize + dequantize->bf16 at int8 G=256 and 6-bit G=32",
-                "elements": 855638016,
-                "l2": "no flush: each launch streams a whole matrix (up to 470 MB)"}
+                "elements": 855638016, "calls": how,
+                "l2": "no flush: each launch streams whole matrices (1.7 GB in, 0.7-0.9 GB out)"}
 
     def setup(self):
         import torch
@@ -942,6 +950,21 @@ class Llama70B:
         zq = self.zq
         out = []
         for b, G in self.schemes:
+            if self.batched:
+                xs = [x for _, _, x in self.mats]
+                cs = [self.buf[(b, G, name)][0] for name, _, _ in self.mats]
+                ss = [self.buf[(b, G, name)][1] for name, _, _ in self.mats]
+                ys = [self.buf[(b, G, name)][2] for name, _, _ in self.mats]
+                ns = [n for _, n, _ in self.mats]
+                nb = sum(2 * n + packed_bytes(b, n, G) for n in ns)
+                out.append(Launch(f"quantize bf16 int{b} G={G} layer (one multi-tensor call)",
+                                  "quantize", nb,
+                                  lambda xs=xs, b=b, G=G, cs=cs, ss=ss: zq.quantize_multi(xs, b, G, cs, ss)))
+                out.append(Launch(f"dequantize int{b} G={G} bf16 layer (one multi-tensor call)",
+                                  "dequantize", nb,
+                                  lambda cs=cs, ss=ss, ns=ns, b=b, G=G, ys=ys: zq.dequantize_multi(
+                                      cs, ss, ns, b, G, outs=ys)))
+                continue
             for name, n, x in self.mats:
                 c, s, y = self.buf[(b, G, name)]
                 nb = 2 * n + packed_bytes(b, n, G)
@@ -1022,6 +1045,13 @@ class Llama70B:
         nbytes = sum(2 * (2 * sample + packed_bytes(b, sample, G)) for b, G in self.schemes)
         return run, nbytes, (f"first {sample:,} elements of the q projection, int8 G=256 and 6-bit "
                              "G=32 round trips, single thread")
+
+
+class Llama70BBatched(Llama70B):
+    """The Llama-3-70B layer round trip through the multi-tensor calls (4 launches a step)."""
+
+    name = "llama70b_batched"
+    batched = True
 
 
 class Llama70BGemm:
@@ -1315,7 +1345,7 @@ class AquavitSchedule:
 
 WORKLOADS = {"gm_sweep": GMSweep, "qwz_fp16": QwzFP16, "qgz_reduce": QgzReduce,
              "agoq_fp8": AgoqFP8, "llama70b": Llama70B, "qgz_two_hop": QgzTwoHop,
-             "llama70b_gemm": Llama70BGemm,
+             "llama70b_gemm": Llama70BGemm, "llama70b_batched": Llama70BBatched,
              "aquavit_schedule": AquavitSchedule, "ring_study": RingStudy}
 
 
@@ -1492,8 +1522,10 @@ def time_cpu_all_cores(wl, sample):
 # The configurations timed after the headline workload in the same run (the
 # other single-GPU workloads of the method: the batched 1 Mi fp16 round trip,
 # the granularity sweep, the qgZ reduce and the AGoQ FP8 accumulate + reduce;
-# then the dequantization fused into the consumer GEMM).
-EXTRA_CONFIGS = ("qwz_fp16", "gm_sweep", "qgz_reduce", "agoq_fp8", "llama70b_gemm")
+# the headline layer again through the multi-tensor calls; then the
+# dequantization fused into the consumer GEMM).
+EXTRA_CONFIGS = ("qwz_fp16", "gm_sweep", "qgz_reduce", "agoq_fp8", "llama70b_batched",
+                 "llama70b_gemm")
 EXTRA_STEPS = 20  # timed steps per extra configuration (at most --steps)
 NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, the ~8 TB/s nominal figure
 

@@ -74,6 +74,8 @@ def _declare(L):
     L.zq_gemm_dequant.restype = i32
     L.zq_quantize_multi.argtypes = [vp, vp, i32, i32, i32, i64, vp, vp, vp]
     L.zq_quantize_multi.restype = i32
+    L.zq_dequantize_multi.argtypes = [vp, vp, vp, i32, i32, i64, vp, i32, vp]
+    L.zq_dequantize_multi.restype = i32
     L.zq_wait_selftest.argtypes = [i64, vp]
     L.zq_wait_selftest.restype = i32
     for f in ("zq_quantize", "zq_dequantize", "zq_reduce_quantized", "zq_fp8_accumulate"):
@@ -474,3 +476,35 @@ def quantize_multi(srcs, fmt: int, G: int, codes=None, scales=None, stream=None)
     _check(lib().zq_quantize_multi(sp, ns, k, dtype_code(dt), fmt, G, cp, kp,
                                    _stream(srcs[0], stream)), "zq_quantize_multi")
     return codes, scales
+
+
+def dequantize_multi(codes_list, scales_list, ns, fmt: int, G: int, out_dtype=None, outs=None,
+                     stream=None):
+    """zq_dequantize of every (codes, scales, n) in one batched call
+    (zq_dequantize_multi). Returns the list of outputs (allocated when not
+    given; float32 unless out_dtype says otherwise)."""
+    torch = _torch()
+    codes_list, scales_list, ns = list(codes_list), list(scales_list), [int(v) for v in ns]
+    k = len(ns)
+    if k == 0:
+        return []
+    if len(codes_list) != k or len(scales_list) != k:
+        raise ValueError("need one codes and one scales tensor per size")
+    dev = codes_list[0].device
+    if outs is None:
+        outs = [torch.empty(n, dtype=out_dtype or torch.float32, device=dev) for n in ns]
+    dt = outs[0].dtype
+    for c, s, n, o in zip(codes_list, scales_list, ns, outs):
+        _need_pair(c, s, fmt, n, G, "input")
+        _cuda_contig(o, "out")
+        if o.dtype != dt or o.numel() < n:
+            raise ValueError("outputs must share one dtype and hold n elements")
+
+    def arr(ts):
+        return (ctypes.c_void_p * k)(*[t.data_ptr() for t in ts])
+
+    cp, sp, op = arr(codes_list), arr(scales_list), arr(outs)
+    nv = (ctypes.c_int64 * k)(*ns)
+    _check(lib().zq_dequantize_multi(cp, sp, nv, k, fmt, G, op, dtype_code(dt),
+                                     _stream(codes_list[0], stream)), "zq_dequantize_multi")
+    return outs

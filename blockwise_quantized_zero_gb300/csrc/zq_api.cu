@@ -298,6 +298,58 @@ zq_status zq_quantize_multi(const void *const *src, const int64_t *n, int count,
   return flush();
 }
 
+zq_status zq_dequantize_multi(const void *const *codes, const float *const *scales,
+                              const int64_t *n, int count, int format, int64_t G, void *const *dst,
+                              int dst_dtype, void *stream) {
+  if (!bits_of(format) || !elem_bytes(dst_dtype)) return ZQ_ERR_UNSUPPORTED;
+  if (count < 0 || !valid_block(G)) return ZQ_ERR_INVALID_ARG;
+  if (count == 0) return ZQ_OK;
+  if (!codes || !scales || !n || !dst) return ZQ_ERR_INVALID_ARG;
+  std::vector<Range> ins, outs;
+  bool wide = true;
+  for (int k = 0; k < count; ++k) {
+    if (n[k] < 0) return ZQ_ERR_INVALID_ARG;
+    if (n[k] == 0) continue;
+    if (!codes[k] || !scales[k] || !dst[k]) return ZQ_ERR_INVALID_ARG;
+    if (!aligned16(codes[k]) || !aligned16(scales[k]) || !aligned16(dst[k])) return ZQ_ERR_MISALIGNED;
+    if (!aligned32(dst[k])) wide = false;
+    ins.emplace_back(codes[k], zq_codes_bytes(format, n[k]));
+    ins.emplace_back(scales[k], size_t(zq_num_blocks(n[k], G)) * 4u);
+    outs.emplace_back(dst[k], size_t(n[k]) * elem_bytes(dst_dtype));
+  }
+  if (any_output_overlap(std::move(ins), std::move(outs))) return ZQ_ERR_ALIAS;
+  for (int k = 0; k < count; ++k) {
+    if (n[k] == 0) continue;
+    for (const void *p : {codes[k], static_cast<const void *>(scales[k]),
+                          static_cast<const void *>(dst[k])})
+      if (zq_status st = check_device_ptr(p)) return st;
+  }
+  DequantMultiArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.log2G = log2_block(G);
+  a.wide = wide ? 1 : 0;
+  int m = 0;
+  auto flush = [&]() -> zq_status {
+    if (m == 0) return ZQ_OK;
+    a.count = m;
+    const zq_status st = from_cuda(launch_dequantize_multi(a, format, dst_dtype, as_stream(stream)));
+    m = 0;
+    return st;
+  };
+  a.tile0[0] = 0;
+  for (int k = 0; k < count; ++k) {
+    if (n[k] == 0) continue;
+    a.codes[m] = static_cast<const uint8_t *>(codes[k]);
+    a.scales[m] = scales[k];
+    a.dst[m] = dst[k];
+    a.n[m] = n[k];
+    a.tile0[m + 1] = a.tile0[m] + n[k] / kTile;
+    if (++m == kMultiMax)
+      if (zq_status st = flush()) return st;
+  }
+  return flush();
+}
+
 zq_status zq_quantize_reordered(const void *src, int src_dtype, int64_t n, int format, int64_t G,
                                 int nodes, int gpus_per_node, void *codes, float *scales,
                                 void *stream) {

@@ -85,6 +85,7 @@ cudaError_t launch_quantize(const void *src, int dt, int64_t n, int fmt, int64_t
                             const SliceRemap &rm = SliceRemap{1, 1, 0});
 // One launch over up to kMultiMax tensors (same type, format and block size).
 cudaError_t launch_quantize_multi(const MultiArgs &a, int dt, int fmt, int64_t G, cudaStream_t st);
+cudaError_t launch_dequantize_multi(const DequantMultiArgs &a, int fmt, int dt, cudaStream_t st);
 cudaError_t launch_dequantize(const void *codes, const float *scales, int64_t n, int fmt,
                               int64_t G, void *dst, int dt, cudaStream_t st, bool wide);
 // The metadata-interleaved record layout (integer codes).

@@ -510,6 +510,84 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t *__r
   }
 }
 
+// ---------------------------------------------------------------------------
+// Multi-tensor dequantize: the dequantize kernel over a list of tensors (same
+// format, block size and output type), their full tiles numbered
+// consecutively and walked in grid-stride order with the same ring of tiles
+// in flight; each ring slot remembers its tile's tensor. Each tensor's
+// partial last tile goes to warp k % nwarps.
+// ---------------------------------------------------------------------------
+struct DequantMultiArgs {
+  const uint8_t *codes[kMultiMax];
+  const float *scales[kMultiMax];
+  void *dst[kMultiMax];
+  int64_t n[kMultiMax];
+  int64_t tile0[kMultiMax + 1];  // prefix sums of full tiles
+  int count;
+  int log2G;
+  int wide;
+};
+
+template <int FMT, int DT>
+__global__ void __launch_bounds__(kThreads) dequantize_multi_kernel(
+    const __grid_constant__ DequantMultiArgs a) {
+  constexpr int B = Fmt<FMT>::kBits, W = Fmt<FMT>::kWords16;
+  const WarpCursor c;
+  const int64_t total = a.tile0[a.count];
+  const bool wd = a.wide != 0;
+  const int lg = a.log2G;
+  constexpr int PF = kDequantAhead<FMT>;
+  uint32_t w[PF][kU][W];
+  float s[PF][kU];
+  int ks[PF];
+  int kl = 0;  // tensor of the last tile loaded (tiles are loaded in increasing order)
+  auto load = [&](int64_t tile, uint32_t (&wd_)[kU][W], float (&sd_)[kU], int &k_) {
+    while (tile >= a.tile0[kl + 1]) ++kl;
+    k_ = kl;
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const int64_t e = (tile - a.tile0[kl]) * kTile + j * kRun + c.lane * kVec;
+      load_codes16<B>(a.codes[kl] + e * B / 8, wd_[j]);
+      sd_[j] = ld_nc_f32(a.scales[kl] + (e >> lg));
+    }
+  };
+#pragma unroll
+  for (int k = 0; k < PF; ++k) {
+    ks[k] = 0;
+    if (c.warp + k * c.nwarps < total) load(c.warp + k * c.nwarps, w[k], s[k], ks[k]);
+  }
+  for (int64_t t = c.warp; t < total;) {
+#pragma unroll
+    for (int k = 0; k < PF; ++k) {  // slot k holds tile t
+      if (t < total) {
+        uint32_t wc[kU][W];
+        float sc[kU];
+        const int kt = ks[k];
+#pragma unroll
+        for (int j = 0; j < kU; ++j) {
+          sc[j] = s[k][j];
+#pragma unroll
+          for (int q = 0; q < W; ++q) wc[j][q] = w[k][j][q];
+        }
+        const int64_t tn = t + PF * c.nwarps;
+        if (tn < total) load(tn, w[k], s[k], ks[k]);
+        const int64_t e0 = (t - a.tile0[kt]) * kTile;
+#pragma unroll
+        for (int j = 0; j < kU; ++j) {
+          float y[kVec];
+          dequant16<FMT>(wc[j], sc[j], y);
+          store16<DT>(a.dst[kt], e0 + j * kRun + c.lane * kVec, y, wd);
+        }
+        t += c.nwarps;
+      }
+    }
+  }
+  for (int kk = int(c.warp); kk < a.count; kk += int(c.nwarps)) {
+    for (int64_t i = (a.n[kk] / kTile) * kTile + c.lane; i < a.n[kk]; i += 32)
+      store1<DT>(a.dst[kk], i, dequant1<FMT>(a.codes[kk], i, a.scales[kk][i >> lg]));
+  }
+}
+
 // ===========================================================================
 // Quantized reduce: acc = +0; acc = fl(acc + fl(D(shard r))) for r in order;
 // then requantize acc with (FOUT, Gout).

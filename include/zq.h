@@ -143,6 +143,22 @@ zq_status zq_quantize_multi(const void *const *src, const int64_t *n, int count,
                             void *stream);
 
 /*
+ * zq_dequantize_multi -- zq_dequantize of `count` tensors in as few launches
+ * as possible (one per 256 tensors), with the same results as `count`
+ * separate calls (a library entry point with no counterpart on the pages;
+ * nothing is allocated).
+ *   codes, scales, n, dst  HOST arrays of `count` entries: tensor k's n[k]
+ *             codes and scales (device, zq_quantize's layout) and its output
+ *             dst[k] (device, n[k] elements of dst_dtype); n[k] = 0 allowed
+ *   format, G, dst_dtype   shared by all tensors
+ * Errors as zq_dequantize, checked for every tensor before anything is
+ * enqueued; no output may overlap any input or any other output.
+ */
+zq_status zq_dequantize_multi(const void *const *codes, const float *const *scales,
+                              const int64_t *n, int count, int format, int64_t G, void *const *dst,
+                              int dst_dtype, void *stream);
+
+/*
  * zq_dequantize -- inverse of zq_quantize ([ZeRO++] qwZ: dequantize after the
  * gather; qgZ: dequantize before the full-precision reduction).
  *   codes, scales  device, as written by zq_quantize(format, G)

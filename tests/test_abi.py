@@ -280,3 +280,23 @@ def test_quantize_multi_argument_errors(L):
     assert call([s0, s1], [1024, 1024], [c0, s0], [k0, k1]) == ALIAS         # output on an input
     assert call([s0, s1], [1024, 1024], [c0, c1], [k0, c1 + 128]) == ALIAS   # scales on codes
     assert call([s0, s0], [1024, 1024], [c0, c1], [k0, k1]) != ALIAS         # shared input is fine
+
+
+def test_dequantize_multi_argument_errors(L):
+    def call(codes, scales, ns, dsts, fmt=O.INT8, dt=O.BF16, G=256, count=None):
+        k = len(ns) if count is None else count
+        arr = lambda xs: (ctypes.c_void_p * max(1, len(xs)))(*xs)  # noqa: E731
+        return L.zq_dequantize_multi(arr(codes), arr(scales), (ctypes.c_int64 * max(1, len(ns)))(*ns), k,
+                                     fmt, G, arr(dsts), dt, None)
+
+    c0, c1 = BASE, BASE + (1 << 24)
+    s0, s1 = BASE + (2 << 24), BASE + (3 << 24)
+    d0, d1 = BASE + (4 << 24), BASE + (5 << 24)
+    assert call([c0], [s0], [1024], [d0], fmt=3) == UNSUPPORTED
+    assert call([c0], [s0], [1024], [d0], dt=9) == UNSUPPORTED
+    assert call([c0], [s0], [1024], [d0], count=-2) == INVALID
+    assert call([c0], [s0], [1024], [d0], count=0) == OK
+    assert call([c0, c1], [s0, s1], [1024, -1], [d0, d1]) == INVALID
+    assert call([c0, c1], [s0, s1], [1024, 1024], [d0, d1 + 4]) == MISALIGNED
+    assert call([c0, c1], [s0, s1], [1024, 1024], [d0, d0 + 1024]) == ALIAS   # outputs overlap
+    assert call([c0, c1], [s0, s1], [1024, 1024], [d0, c1]) == ALIAS          # output on codes

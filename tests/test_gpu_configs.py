@@ -161,24 +161,32 @@ def test_agoq_fp8_full(zq):
 
 def test_llama70b_layer_full(zq):
     """The seven Llama-3-70B layer matrices, int8 G=256 and 6-bit G=32, quantize
-    + dequantize -> bf16: every element of every matrix."""
+    + dequantize -> bf16, in the benchmark's form (one multi-tensor quantize
+    and one multi-tensor dequantize call per scheme): every element of every
+    matrix against the oracle; the per-matrix calls give the same bytes."""
     import torch
 
     from blockwise_quantized_zero_gb300 import inputs
 
     t0 = time.time()
-    total = checked = 0
-    for name, r, c, bits in inputs.llama70b_layer_bf16():
-        n = r * c
-        total += n
-        xd = bf16_dev(bits)
-        for b, G in ((8, 256), (6, 32)):
-            dc, ds = zq.quantize(xd, b, G)
-            y = zq.dequantize(dc, ds, n, b, G, out_dtype=torch.bfloat16)
+    layer = list(inputs.llama70b_layer_bf16())
+    xds = [bf16_dev(bits) for _, _, _, bits in layer]
+    ns = [r * c for _, r, c, _ in layer]
+    assert sum(ns) == 855638016
+    checked = 0
+    for b, G in ((8, 256), (6, 32)):
+        cs, ss = zq.quantize_multi(xds, b, G)
+        ys = zq.dequantize_multi(cs, ss, ns, b, G, out_dtype=torch.bfloat16)
+        for (name, r, c, bits), dc, ds, y, xd in zip(layer, cs, ss, ys, xds):
             checked += F.check_roundtrip(f"{name} b={b} G={G}", bits, O.BF16, b, G, to_host(dc),
                                          to_host(ds), to_host(y), O.BF16)
-            del dc, ds, y
-        del xd
-    assert total == 855638016 and checked == 2 * total
+            c1, s1 = zq.quantize(xd, b, G)
+            assert torch.equal(c1, dc) and torch.equal(s1.view(torch.int32), ds.view(torch.int32)), name
+            y1 = zq.dequantize(c1, s1, r * c, b, G, out_dtype=torch.bfloat16)
+            assert torch.equal(y1.view(torch.int16), y.view(torch.int16)), name
+            del c1, s1, y1
+        del cs, ss, ys
+    assert checked == 2 * sum(ns)
+    del xds
     torch.cuda.empty_cache()
-    _report("llama70b (2 schemes, quantize + dequantize)", checked, t0)
+    _report("llama70b (2 schemes, batched quantize + dequantize; per-matrix calls equal)", checked, t0)
