@@ -1343,9 +1343,31 @@ class AquavitSchedule:
         return run, nbytes, desc
 
 
+class Llama70BGemmFew(Llama70BGemm):
+    """The same fused GEMM on 128 tokens (a few-token forward: decode or a
+    small micro-batch). Every projection has fewer 128-row output tiles than
+    the GPU has SMs, so the launcher splits K over clusters of CTAs (128 x 256
+    tiles, 4 CTAs a tile, for q, o and down; 128 x 128 tiles, 8 CTAs, for k
+    and v; 256 x 128 unsplit tiles for gate and up). At 128 tokens an int8
+    weight byte carries 256 flops, so the weights' HBM time and the tensor
+    time are about equal; both rooflines are reported."""
+
+    name = "llama70b_gemm_t128"
+    M = 128
+
+    def config(self):
+        c = super().config()
+        c["workload"] = ("llama70b_gemm_t128: the seven projections of one Llama-3-70B decoder layer "
+                         "(855,638,016 weights, int8 G=256) on 128 bf16 tokens, dequantization fused "
+                         "into the tcgen05 GEMM, K split over clusters where the tiles are too few")
+        c["l2"] = "no flush: 0.9 GB of int8 weights per step >> 126 MB L2"
+        return c
+
+
 WORKLOADS = {"gm_sweep": GMSweep, "qwz_fp16": QwzFP16, "qgz_reduce": QgzReduce,
              "agoq_fp8": AgoqFP8, "llama70b": Llama70B, "qgz_two_hop": QgzTwoHop,
-             "llama70b_gemm": Llama70BGemm, "llama70b_batched": Llama70BBatched,
+             "llama70b_gemm": Llama70BGemm, "llama70b_gemm_t128": Llama70BGemmFew,
+             "llama70b_batched": Llama70BBatched,
              "aquavit_schedule": AquavitSchedule, "ring_study": RingStudy}
 
 
@@ -1523,9 +1545,9 @@ def time_cpu_all_cores(wl, sample):
 # other single-GPU workloads of the method: the batched 1 Mi fp16 round trip,
 # the granularity sweep, the qgZ reduce and the AGoQ FP8 accumulate + reduce;
 # the headline layer again through the multi-tensor calls; then the
-# dequantization fused into the consumer GEMM).
+# dequantization fused into the consumer GEMM, on 4096 and on 128 tokens).
 EXTRA_CONFIGS = ("qwz_fp16", "gm_sweep", "qgz_reduce", "agoq_fp8", "llama70b_batched",
-                 "llama70b_gemm")
+                 "llama70b_gemm", "llama70b_gemm_t128")
 EXTRA_STEPS = 20  # timed steps per extra configuration (at most --steps)
 NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, the ~8 TB/s nominal figure
 

@@ -72,6 +72,9 @@ def _declare(L):
     L.zq_fp8_accumulate.argtypes = [vp, vp, vp, i32, i64, i64, vp]
     L.zq_gemm_dequant.argtypes = [vp, i64, i64, vp, vp, i32, i64, i64, vp, i32, vp]
     L.zq_gemm_dequant.restype = i32
+    L.zq_gemm_plan.argtypes = [i64, i64, i64, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                               ctypes.POINTER(ctypes.c_int)]
+    L.zq_gemm_plan.restype = i32
     L.zq_quantize_multi.argtypes = [vp, vp, i32, i32, i32, i64, vp, vp, vp]
     L.zq_quantize_multi.restype = i32
     L.zq_dequantize_multi.argtypes = [vp, vp, vp, i32, i32, i64, vp, i32, vp]
@@ -445,6 +448,16 @@ def gemm_dequant(x, w_codes, w_scales, fmt: int, G: int, N: int, out_dtype=None,
                                  G, N, out.data_ptr(), dtype_code(out.dtype), _stream(x, stream)),
            "zq_gemm_dequant")
     return out
+
+
+def gemm_plan(M: int, N: int, K: int):
+    """The output tile gemm_dequant uses for an M x N x K problem on the
+    current device: (rows, columns, CTAs sharing a tile's K range)
+    (zq_gemm_plan)."""
+    bm, bn, sp = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(lib().zq_gemm_plan(int(M), int(N), int(K), ctypes.byref(bm), ctypes.byref(bn),
+                              ctypes.byref(sp)), "zq_gemm_plan")
+    return bm.value, bn.value, sp.value
 
 
 def quantize_multi(srcs, fmt: int, G: int, codes=None, scales=None, stream=None):

@@ -731,6 +731,17 @@ zq_status zq_gemm_dequant(const void *x, int64_t M, int64_t K, const void *w_cod
                                        as_stream(stream)));
 }
 
+zq_status zq_gemm_plan(int64_t M, int64_t N, int64_t K, int *bm, int *bn, int *split) {
+  if (!bm || !bn || !split || M < 0 || N <= 0 || K <= 0 || N % 64 != 0 || K % 64 != 0)
+    return ZQ_ERR_INVALID_ARG;
+  int a = 128, b = 64, c = 1;
+  gemm_tile_shape(M, N, K, a, b, c);
+  *bm = a;
+  *bn = b;
+  *split = c;
+  return ZQ_OK;
+}
+
 zq_status zq_fp8_accumulate(void *main_codes, float *main_scales, const void *grad, int grad_dtype,
                             int64_t n, int64_t G, void *stream) {
   if (!elem_bytes(grad_dtype)) return ZQ_ERR_UNSUPPORTED;

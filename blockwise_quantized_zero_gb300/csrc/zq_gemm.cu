@@ -7,11 +7,15 @@
 
 namespace zq {
 
-template <int FMT, int BN, int BM, int OUT>
+// SPLIT: launched in clusters of CS CTAs (split-K, one output tile per
+// cluster); otherwise persistent, one CTA per SM.
+template <int FMT, int BN, int BM, int OUT, bool SPLIT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_dequant_kernel(const __grid_constant__ CUtensorMap tm_x,
                         const __grid_constant__ CUtensorMap tm_codes, const GemmArgs a) {
   using GG = GemmGeom<FMT, BN, BM>;
+  static_assert(!SPLIT || BM == kGemmMmaM, "split-K tiles have one 128-row half");
+  static_assert(!SPLIT || GG::kPartBytes <= GG::kBarOff, "partial sums fit the stage memory");
   constexpr int S = GG::kStages, NB = GG::kBRing, NACC = GG::kAccs, H = GG::kHalves;
   constexpr int BITS = GG::kBits;
   extern __shared__ uint8_t gemm_smem_raw[];
@@ -39,6 +43,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = a.tiles_m * a.tiles_n;
   const int KB = int(a.K / kGemmBK);
+  // Work of this CTA: tiles t0, t0 + tstep, ... and k-blocks [kb0, kb1) of each.
+  const int cs = SPLIT ? int(tc::cluster_size()) : 1;
+  const int rank = SPLIT ? int(tc::cluster_rank()) : 0;
+  const int t0 = SPLIT ? int(blockIdx.x) / cs : int(blockIdx.x);
+  const int tstep = SPLIT ? ntiles : int(gridDim.x);
+  const int kb0 = int(int64_t(rank) * KB / cs), kb1 = int(int64_t(rank + 1) * KB / cs);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -73,10 +83,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc::tma_prefetch_desc(&tm_codes);
       uint32_t u = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      for (int t = t0; t < ntiles && ok; t += tstep) {
         int mb, nb;
         gemm_tile(t, a.tiles_m, a.tiles_n, mb, nb);
-        for (int kb = 0; kb < KB; ++kb, ++u) {
+        for (int kb = kb0; kb < kb1; ++kb, ++u) {
           const int s = int(u % S);
           const uint32_t r = u / S;
           if (r >= 1 && !gemm_wait_thread(empty(s), (r - 1) & 1u, abort)) {
@@ -101,13 +111,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t u = 0;
       int i = 0;
       bool ok = true, issued = false;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++i) {
+      for (int t = t0; t < ntiles && ok; t += tstep, ++i) {
         const int ab = i % NACC;
         const uint32_t ra = uint32_t(i / NACC);
         if (ra >= 1 && !gemm_wait_thread(acc_empty(ab), (ra - 1) & 1u, abort)) break;
         tc::fence_after_sync();
         const uint32_t d = tmem + uint32_t(ab * GG::kAccCols);
-        for (int kb = 0; kb < KB; ++kb, ++u) {
+        for (int kb = kb0; kb < kb1; ++kb, ++u) {
           const int s = int(u % S), b = int(u % NB);
           if (!gemm_wait_thread(full(s), (u / S) & 1u, abort) ||
               !gemm_wait_thread(bready(b), (u / NB) & 1u, abort)) {
@@ -122,7 +132,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int k4 = 0; k4 < kGemmBK / 16; ++k4)  // +32 bytes along K per step
               tc::mma_bf16(d + uint32_t(h * BN), ad + 2u * k4, bd + 2u * k4, idesc,
-                           (kb | k4) != 0 ? 1u : 0u);
+                           (kb != kb0 || k4 != 0) ? 1u : 0u);
           }
           tc::mma_commit(empty(s));
           tc::mma_commit(bfree(b));
@@ -159,7 +169,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int kpp = lg <= 6 ? 1 : 1 << (lg - 6);  // k-blocks per block
     // Cursor one k-block ahead of the dequantization: tile f_t, k-block f_kb,
     // each task's element index at k = 0.
-    int f_t = blockIdx.x, f_kb = 0;
+    int f_t = t0, f_kb = kb0;
     int64_t f_e[T];
     auto f_tile = [&]() {
       if (f_t < ntiles) {
@@ -171,9 +181,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     };
     auto f_next = [&]() {
-      if (++f_kb == KB) {
-        f_kb = 0;
-        f_t += gridDim.x;
+      if (++f_kb == kb1) {
+        f_kb = kb0;
+        f_t += tstep;
         f_tile();
       }
     };
@@ -183,13 +193,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int i = 0; i < T; ++i) {
       cur[i] = 0.0f;
       nxt[i] = 0.0f;
-      if (owner && dt + i * kGemmDqThreads < GG::kTasks) cur[i] = ld_nc_f32(a.scales + (f_e[i] >> lg));
+      if (owner && dt + i * kGemmDqThreads < GG::kTasks && f_t < ntiles)
+        cur[i] = ld_nc_f32(a.scales + ((f_e[i] + int64_t(kb0) * kGemmBK) >> lg));
     }
     f_next();
     uint32_t u = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-      for (int kb = 0; kb < KB; ++kb, ++u) {
+    for (int t = t0; t < ntiles && ok; t += tstep) {
+      for (int kb = kb0; kb < kb1; ++kb, ++u) {
         const int s = int(u % S), b = int(u % NB);
         const bool fresh = f_t < ntiles && f_kb % kpp == 0;  // the next k-block starts a block
         if (fresh && owner) {
@@ -240,8 +251,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ---------------- epilogue: tensor memory -> y ----------------
     const int q = w & 3;  // this warp may read TMEM lanes [32q, 32q + 32)
+    if constexpr (SPLIT) {
+      // one tile: copy the partial sums (row 32q + lane) to shared memory
+      if (t0 < ntiles && gemm_wait_warp(acc_full(0), 0u, abort)) {
+        tc::fence_after_sync();
+        const uint32_t row = base + uint32_t((q * 32 + lane) * GG::kPartStride * 4);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          tc::tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(c), v);
+#pragma unroll
+          for (int k = 0; k < 32; k += 4)
+            tc::st_shared_v4(row + uint32_t((c + k) * 4), v[k], v[k + 1], v[k + 2], v[k + 3]);
+        }
+      }
+      tc::fence_before_sync();
+    }
     int i = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+    for (int t = t0; t < ntiles && !SPLIT; t += tstep, ++i) {
       int mb, nb;
       gemm_tile(t, a.tiles_m, a.tiles_n, mb, nb);
       const int ab = i % NACC;
@@ -283,6 +310,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   }
 
+  if constexpr (SPLIT) {
+    tc::cluster_sync();  // every CTA's partial sums are in its shared memory
+    if (w >= 2 + kGemmDequantWarps && t0 < ntiles) {
+      // rows [rank * 128 / cs, (rank + 1) * 128 / cs) of the tile: the sum of
+      // the cs partial tiles in rank order, 4 columns a lane
+      int mb, nb;
+      gemm_tile(t0, a.tiles_m, a.tiles_n, mb, nb);
+      const int rows = kGemmMmaM / cs, ew = w - (2 + kGemmDequantWarps);
+      for (int r = rank * rows + ew; r < (rank + 1) * rows; r += kGemmEpiWarps) {
+        const int64_t m = int64_t(mb) * BM + r;
+        if (m >= a.M) break;
+        for (int c = lane * 4; c < BN; c += 128) {
+          const uint32_t off = base + uint32_t((r * GG::kPartStride + c) * 4);
+          float x0, x1, x2, x3;
+          tc::ld_cluster_v4(tc::peer_addr(off, 0), x0, x1, x2, x3);
+          for (int p = 1; p < cs; ++p) {
+            float y0, y1, y2, y3;
+            tc::ld_cluster_v4(tc::peer_addr(off, uint32_t(p)), y0, y1, y2, y3);
+            x0 = __fadd_rn(x0, y0);
+            x1 = __fadd_rn(x1, y1);
+            x2 = __fadd_rn(x2, y2);
+            x3 = __fadd_rn(x3, y3);
+          }
+          const int64_t o = m * a.N + int64_t(nb) * BN + c;
+          if constexpr (OUT == DT_F32) {
+            st_v4(static_cast<uint32_t *>(a.y) + o, __float_as_uint(x0), __float_as_uint(x1),
+                  __float_as_uint(x2), __float_as_uint(x3));
+          } else {
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(x0, x1), h1 = __floats2bfloat162_rn(x2, x3);
+            uint2 *dst = reinterpret_cast<uint2 *>(static_cast<uint16_t *>(a.y) + o);
+            *dst = make_uint2(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1));
+          }
+        }
+      }
+    }
+    tc::cluster_sync();  // no CTA leaves while its partial sums may still be read
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -332,10 +396,11 @@ cudaError_t make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, ui
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int FMT, int BN, int BM, int OUT>
-cudaError_t go_gemm(const void *x, const void *codes, const GemmArgs &a, cudaStream_t st) {
+template <int FMT, int BN, int BM, int OUT, bool SPLIT = false>
+cudaError_t go_gemm(const void *x, const void *codes, const GemmArgs &a, int split,
+                    cudaStream_t st) {
   using GG = GemmGeom<FMT, BN, BM>;
-  constexpr auto K = gemm_dequant_kernel<FMT, BN, BM, OUT>;
+  constexpr auto K = gemm_dequant_kernel<FMT, BN, BM, OUT, SPLIT>;
   static const cudaError_t attr =
       cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, GG::kSmem);
   if (attr != cudaSuccess) return attr;
@@ -350,63 +415,177 @@ cudaError_t go_gemm(const void *x, const void *codes, const GemmArgs &a, cudaStr
                BN, GG::kCodeRow, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   const int tiles = a.tiles_m * a.tiles_n;
-  const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
-  K<<<grid, kGemmThreads, GG::kSmem, st>>>(tx, tcd, a);
-  return cudaGetLastError();
+  if constexpr (SPLIT) {  // one cluster of `split` CTAs per output tile
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(unsigned(tiles * split));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = GG::kSmem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, K, tx, tcd, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  } else {
+    (void)split;
+    const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
+    K<<<grid, kGemmThreads, GG::kSmem, st>>>(tx, tcd, a);
+    return cudaGetLastError();
+  }
 }
 
 // The tile shapes built: 256 x 256 and 256 x 128 for problems with enough
 // rows, 128 x 128 and 128 x 64 otherwise.
 template <int FMT, int OUT>
 cudaError_t go_gemm_shape(const void *x, const void *codes, const GemmArgs &a, int bm, int bn,
-                          cudaStream_t st) {
-  if (bm == 256 && bn == 256) return go_gemm<FMT, 256, 256, OUT>(x, codes, a, st);
-  if (bm == 256 && bn == 128) return go_gemm<FMT, 128, 256, OUT>(x, codes, a, st);
-  if (bm == 128 && bn == 128) return go_gemm<FMT, 128, 128, OUT>(x, codes, a, st);
-  if (bm == 128 && bn == 64) return go_gemm<FMT, 64, 128, OUT>(x, codes, a, st);
+                          int split, cudaStream_t st) {
+  if (split > 1) {
+    if (bm == 128 && bn == 256) return go_gemm<FMT, 256, 128, OUT, true>(x, codes, a, split, st);
+    if (bm == 128 && bn == 128) return go_gemm<FMT, 128, 128, OUT, true>(x, codes, a, split, st);
+    return cudaErrorInvalidValue;
+  }
+  if (bm == 256 && bn == 256) return go_gemm<FMT, 256, 256, OUT>(x, codes, a, 1, st);
+  if (bm == 256 && bn == 128) return go_gemm<FMT, 128, 256, OUT>(x, codes, a, 1, st);
+  if (bm == 128 && bn == 128) return go_gemm<FMT, 128, 128, OUT>(x, codes, a, 1, st);
+  if (bm == 128 && bn == 64) return go_gemm<FMT, 64, 128, OUT>(x, codes, a, 1, st);
   return cudaErrorInvalidValue;
 }
 
 template <int OUT>
 cudaError_t go_gemm_fmt(const void *x, const void *codes, const GemmArgs &a, int fmt, int bm,
-                        int bn, cudaStream_t st) {
+                        int bn, int split, cudaStream_t st) {
   switch (fmt) {
-    case F_INT2: return go_gemm_shape<F_INT2, OUT>(x, codes, a, bm, bn, st);
-    case F_INT4: return go_gemm_shape<F_INT4, OUT>(x, codes, a, bm, bn, st);
-    case F_INT6: return go_gemm_shape<F_INT6, OUT>(x, codes, a, bm, bn, st);
-    case F_INT8: return go_gemm_shape<F_INT8, OUT>(x, codes, a, bm, bn, st);
-    case F_E4M3: return go_gemm_shape<F_E4M3, OUT>(x, codes, a, bm, bn, st);
+    case F_INT2: return go_gemm_shape<F_INT2, OUT>(x, codes, a, bm, bn, split, st);
+    case F_INT4: return go_gemm_shape<F_INT4, OUT>(x, codes, a, bm, bn, split, st);
+    case F_INT6: return go_gemm_shape<F_INT6, OUT>(x, codes, a, bm, bn, split, st);
+    case F_INT8: return go_gemm_shape<F_INT8, OUT>(x, codes, a, bm, bn, split, st);
+    case F_E4M3: return go_gemm_shape<F_E4M3, OUT>(x, codes, a, bm, bn, split, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-// Tile shape: the first of 256 x 256, 256 x 128, 128 x 128 whose column width
-// divides N and that still gives every SM an output tile (taller tiles share
-// one dequantized weight tile between more rows); 128 x 64 for small
-// problems. (128 x 256 would never come first: a problem it gives enough
-// tiles gives 256 x 128 as many.)
-void gemm_tile_shape(int64_t M, int64_t N, int &bm, int &bn) {
-  const int64_t sms = device_sm_count();
-  const int shapes[3][2] = {{256, 256}, {256, 128}, {128, 128}};
-  for (const auto &sh : shapes) {
-    const int64_t tm = (M + sh[0] - 1) / sh[0];
-    if (N % sh[1] == 0 && tm * (N / sh[1]) >= sms) {
-      bm = sh[0];
-      bn = sh[1];
-      return;
-    }
+// CTAs of split-K clusters of `cs` CTAs that can be resident at once
+// (clusters are placed within GPU processing clusters, so fewer than one per
+// SM in general), from the occupancy query of a representative kernel (all
+// split kernels take one CTA an SM); cached per device.
+namespace {
+std::mutex g_cluster_mutex;
+int g_cluster_ctas[64][4];  // [device][log2 cs]
+
+int split_ctas_per_wave(int cs) {
+  const int sms = device_sm_count();
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    return sms / cs * cs;
   }
+  const int li = cs == 2 ? 1 : cs == 4 ? 2 : 3;
+  std::lock_guard<std::mutex> lock(g_cluster_mutex);
+  if (g_cluster_ctas[dev][li] == 0) {
+    constexpr auto K = gemm_dequant_kernel<F_INT8, 256, 128, DT_BF16, true>;
+    using GG = GemmGeom<F_INT8, 256, 128>;
+    int n = 0;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(unsigned(cs * sms));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = GG::kSmem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, GG::kSmem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, K, &cfg) != cudaSuccess || n < 1) {
+      (void)cudaGetLastError();
+      n = sms / cs;
+    }
+    g_cluster_ctas[dev][li] = n * cs;
+  }
+  return g_cluster_ctas[dev][li];
+}
+}  // namespace
+
+// Tile shape. Problems of more than 256 rows: the first of 256 x 256,
+// 256 x 128, 128 x 128 whose column width divides N and that still gives
+// every SM an output tile (taller tiles share one dequantized weight tile
+// between more rows), else 128 x 64. (128 x 256 would never come first: a
+// problem it gives enough tiles gives 256 x 128 as many.)
+// Up to 256 rows (few tokens) the tiles are few and the waves of CTAs
+// decide: each candidate, unsplit (persistent) or split-K over clusters of
+// 2, 4 or 8 CTAs (128-row tiles, at least 4 k-blocks a CTA), is given the
+// time waves x (k-blocks a CTA x time a k-block + fixed time a CTA), with
+// the times measured on GB300 (microseconds a 64-deep k-block: 256 x 256
+// 0.885, 256 x 128 0.60, 128 x 256 0.664, 128 x 128 0.49, 128 x 64 0.42;
+// fixed: 3 unsplit, 11 split, which adds the partial-tile exchange), and the
+// fastest is taken.
+void gemm_tile_shape(int64_t M, int64_t N, int64_t K, int &bm, int &bn, int &split) {
+  const int64_t sms = device_sm_count();
+  split = 1;
+  if (M > 256) {
+    const int shapes[3][2] = {{256, 256}, {256, 128}, {128, 128}};
+    for (const auto &sh : shapes) {
+      const int64_t tm = (M + sh[0] - 1) / sh[0];
+      if (N % sh[1] == 0 && tm * (N / sh[1]) >= sms) {
+        bm = sh[0];
+        bn = sh[1];
+        return;
+      }
+    }
+    bm = 128;
+    bn = 64;
+    return;
+  }
+  const double kb = double(K / kGemmBK);
+  struct Unsplit { int bm, bn; double t; };
+  const Unsplit us[4] = {{256, 256, 0.885}, {256, 128, 0.60}, {128, 128, 0.49}, {128, 64, 0.42}};
+  double best = 1e300;
   bm = 128;
   bn = 64;
+  for (const auto &u : us) {
+    if (N % u.bn != 0) continue;
+    const int64_t tiles = (M + u.bm - 1) / u.bm * (N / u.bn);
+    const double t = double((tiles + sms - 1) / sms) * (kb * u.t) + 3.0;
+    if (t < best) {
+      best = t;
+      bm = u.bm;
+      bn = u.bn;
+    }
+  }
+  struct Split { int bn; double t; };
+  const Split sp[2] = {{256, 0.664}, {128, 0.49}};
+  for (const auto &c : sp) {
+    if (N % c.bn != 0) continue;
+    const int64_t tiles = (M + 127) / 128 * (N / c.bn);
+    for (int cs = 2; cs <= kGemmMaxSplit; cs *= 2) {
+      if (kb < 4.0 * cs) continue;
+      const int64_t wave = split_ctas_per_wave(cs);
+      const double t = double((tiles * cs + wave - 1) / wave) * (kb / cs * c.t + 11.0);
+      if (t < best) {
+        best = t;
+        bm = 128;
+        bn = c.bn;
+        split = cs;
+      }
+    }
+  }
 }
 
 cudaError_t launch_gemm_dequant(const void *x, int64_t M, int64_t K, const void *codes,
                                 const float *scales, int fmt, int64_t G, int64_t N, void *y,
                                 int out_dt, cudaStream_t st) {
-  int bm = 128, bn = 64;
-  gemm_tile_shape(M, N, bm, bn);
+  int bm = 128, bn = 64, split = 1;
+  gemm_tile_shape(M, N, K, bm, bn, split);
   GemmArgs a;
   a.scales = scales;
   a.y = y;
@@ -416,8 +595,8 @@ cudaError_t launch_gemm_dequant(const void *x, int64_t M, int64_t K, const void 
   a.log2G = log2_block(G);
   a.tiles_m = int((M + bm - 1) / bm);
   a.tiles_n = int(N / bn);
-  if (out_dt == DT_F32) return go_gemm_fmt<DT_F32>(x, codes, a, fmt, bm, bn, st);
-  if (out_dt == DT_BF16) return go_gemm_fmt<DT_BF16>(x, codes, a, fmt, bm, bn, st);
+  if (out_dt == DT_F32) return go_gemm_fmt<DT_F32>(x, codes, a, fmt, bm, bn, split, st);
+  if (out_dt == DT_BF16) return go_gemm_fmt<DT_BF16>(x, codes, a, fmt, bm, bn, split, st);
   return cudaErrorInvalidValue;
 }
 

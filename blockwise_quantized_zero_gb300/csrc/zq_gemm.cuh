@@ -52,6 +52,16 @@ constexpr int kGemmWarps = 2 + kGemmDequantWarps + kGemmEpiWarps;
 constexpr int kGemmThreads = kGemmWarps * 32;
 constexpr int kGemmSmemBudget = 220 * 1024;
 
+// Split-K for problems with too few output tiles to fill the GPU (few
+// tokens): a cluster of CS CTAs (2, 4 or 8) shares one 128-row output tile,
+// CTA r taking k-blocks [r KB / CS, (r+1) KB / CS). After its last MMA each
+// CTA copies its accumulator to shared memory; after a cluster barrier, CTA r
+// sums rows [r 128 / CS, (r+1) 128 / CS) of the CS partial tiles, read through
+// distributed shared memory in rank order (a fixed order: the result does not
+// depend on timing), and stores them; a second cluster barrier keeps every
+// CTA resident until its partial sums have been read.
+constexpr int kGemmMaxSplit = 8;
+
 // Output tile BM x BN: BM / 128 MMAs of 128 rows per 16-deep step share the
 // dequantized weight operand (the dequantization work per flop is 1 / 2BM).
 template <int FMT, int BN, int BM> struct GemmGeom {
@@ -82,6 +92,11 @@ template <int FMT, int BN, int BM> struct GemmGeom {
   // per accumulator; drain; then the tmem slot and the abort flag
   static constexpr int kNumBars = 2 * kStages + 2 * kBRing + 2 * kAccs + 1;
   static constexpr int kSmem = 1024 + kBarOff + kNumBars * 8 + 16;
+  // Split-K (one output tile per cluster): each CTA's fp32 partial sums, rows
+  // of BN + 4 words (the padding spreads one row per lane over the banks),
+  // reuse the stage and weight-operand memory once the MMAs are done.
+  static constexpr int kPartStride = BN + 4;
+  static constexpr int kPartBytes = kGemmMmaM * kPartStride * 4;
   static constexpr uint32_t kTxBytes = kABytes + kCBytes;
   static_assert(BM == 128 || BM == 256, "tile rows");
   static_assert(kStages >= 2, "at least two stages");

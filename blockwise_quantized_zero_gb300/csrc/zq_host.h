@@ -114,7 +114,7 @@ unsigned take_reduce_few_device_error();
 cudaError_t launch_gemm_dequant(const void *x, int64_t M, int64_t K, const void *codes,
                                 const float *scales, int fmt, int64_t G, int64_t N, void *y,
                                 int out_dt, cudaStream_t st);
-void gemm_tile_shape(int64_t M, int64_t N, int &bm, int &bn);
+void gemm_tile_shape(int64_t M, int64_t N, int64_t K, int &bm, int &bn, int &split);
 unsigned take_gemm_device_error();
 
 cudaError_t launch_fp8_accumulate(void *codes, float *scales, const void *grad, int dt, int64_t n,

@@ -115,5 +115,44 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// Thread-block clusters: rank, size, peer shared-memory addresses and loads,
+// the cluster barrier (the split-K reduction of the fused GEMM).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared::cluster address of this CTA's shared address `a` in CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t a, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(rank));
+  return d;
+}
+
+// Four fp32 words from the shared memory of any CTA of the cluster (address
+// from peer_addr).
+__device__ __forceinline__ void ld_cluster_v4(uint32_t a, float &x, float &y, float &z, float &w) {
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(x), "=f"(y), "=f"(z), "=f"(w)
+               : "r"(a)
+               : "memory");
+}
+
+// Every thread of every CTA of the cluster arrives and waits (release /
+// acquire at cluster scope). A hardware barrier like __syncthreads: it ends
+// once every thread has arrived, and every wait before it is bounded.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 }  // namespace tc
 }  // namespace zq

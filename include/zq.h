@@ -377,7 +377,10 @@ zq_status zq_fp8_accumulate(void *main_codes, float *main_scales, const void *gr
  *                                         for element n*K + k of W,
  * accumulated in fp32 on the tensor cores (tcgen05, bf16 operands; the order
  * of the fp32 additions is the hardware's), then stored as fp32 or rounded
- * once to bf16. The bf16 weight matrix is never written to memory.
+ * once to bf16. The bf16 weight matrix is never written to memory. Problems
+ * with few rows may split K over a cluster of 2, 4 or 8 CTAs (zq_gemm_plan);
+ * their partial tiles are added in a fixed order, so the result does not
+ * depend on timing either way.
  *   x          device, M x K bf16, row-major (K-major)
  *   w_codes,   device, the zq_quantize output (format, G) of the N x K weight
  *   w_scales   matrix flattened row-major: zq_codes_bytes(format, N*K) bytes
@@ -395,6 +398,16 @@ zq_status zq_fp8_accumulate(void *main_codes, float *main_scales, const void *gr
 zq_status zq_gemm_dequant(const void *x, int64_t M, int64_t K, const void *w_codes,
                           const float *w_scales, int format, int64_t G, int64_t N, void *y,
                           int y_dtype, void *stream);
+
+/*
+ * zq_gemm_plan -- the output tile zq_gemm_dequant uses for an M x N x K
+ * problem on the current device: *bm x *bn rows x columns, and *split CTAs
+ * (one cluster) sharing each tile's K range (1: no split). Host only; it
+ * queries the device's SM count and cluster occupancy once.
+ * Errors: ZQ_ERR_INVALID_ARG for null outputs or sizes zq_gemm_dequant
+ * refuses (M < 0, N or K not a positive multiple of 64).
+ */
+zq_status zq_gemm_plan(int64_t M, int64_t N, int64_t K, int *bm, int *bn, int *split);
 
 /*
  * zq_device_status -- errors the kernels found on the device. The reduce

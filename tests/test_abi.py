@@ -255,6 +255,26 @@ def test_gemm_dequant_argument_errors(L):
     assert g(x, 128, 512, c, s, O.INT8, 128, 256, c + 64, O.BF16, None) == ALIAS
 
 
+def test_gemm_plan(L):
+    """zq_gemm_plan refuses bad sizes and null outputs; a problem with
+    thousands of rows gets an unsplit 256-row tile, one with a hundred rows
+    and a long K a 128-row tile with K split over a cluster. (Without a
+    device the plan uses a default SM count; the choice is the same.)"""
+    p = L.zq_gemm_plan
+    I = ctypes.c_int
+    p.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(I), ctypes.POINTER(I),
+                  ctypes.POINTER(I)]
+    bm, bn, sp = I(), I(), I()
+    out = (ctypes.byref(bm), ctypes.byref(bn), ctypes.byref(sp))
+    assert p(128, 250, 512, *out) == INVALID
+    assert p(128, 256, 500, *out) == INVALID
+    assert p(-1, 256, 512, *out) == INVALID
+    assert p(128, 256, 512, None, out[1], out[2]) == INVALID
+    assert p(4096, 8192, 8192, *out) == OK and (bm.value, bn.value, sp.value) == (256, 256, 1)
+    assert p(128, 8192, 8192, *out) == OK and bm.value == 128 and sp.value in (2, 4, 8)
+    assert p(1, 64, 64, *out) == OK and (bm.value, bn.value, sp.value) == (128, 64, 1)
+
+
 def test_quantize_multi_argument_errors(L):
     """zq_quantize_multi: bad format / type, negative counts and sizes, null,
     misaligned and overlapping buffers are refused before any work."""

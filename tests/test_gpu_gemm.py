@@ -15,7 +15,9 @@ Weights are quantized by the oracle (never by the GPU). Two kinds of check:
 Shapes cover each output tile the launcher picks (256 x 256 with one
 accumulator, 256 x 128, 128 x 128 and 128 x 64 with two), several tiles per
 CTA (the stage ring and the accumulators wrap), a ragged last row tile, every
-code format and several block sizes.
+code format and several block sizes, and the split-K form for few rows
+(128 x 256 and 128 x 128 tiles over clusters of 2, 4 and 8 CTAs; each case
+checks through zq_gemm_plan that the split path is the one taken).
 """
 import numpy as np
 import pytest
@@ -123,6 +125,74 @@ def test_gemm_random_within_fp32_accumulation_bound(zq, M, N, K, fmt, G, out):
     err = np.abs(got - ref)
     worst = float(np.max(err / np.maximum(tol, 1e-300)))
     assert np.all(err <= tol), f"worst error {worst:.3f} of the bound"
+
+
+SPLIT_CASES = [  # few rows: K split over clusters (the plan on GB300 in the comment)
+    (1, 512, 2048, O.INT8, 256),     # 128 x 128 tiles, 8 CTAs a tile
+    (77, 1024, 4096, O.INT4, 128),   # 128 x 128, 8
+    (255, 1024, 8192, O.INT6, 64),   # 128 x 128, 8, two row tiles
+    (1, 6144, 2048, O.INT8, 128),    # 128 x 256, 4
+    (77, 6144, 2048, O.INT2, 32),    # 128 x 256, 4
+    (1, 12288, 4096, O.INT4, 64),    # 128 x 256, 2
+    (200, 6144, 4096, O.E4M3, 512),  # 128 x 256, 2, two row tiles
+    (150, 2048, 4096, O.INT8, 256),  # 128 x 256, 8, two row tiles
+    (1, 3072, 2048, O.INT6, 32),     # 128 x 256, 8
+]
+
+
+@pytest.mark.parametrize("M,N,K,fmt,G", SPLIT_CASES)
+def test_gemm_split_k_exact_small_integers(zq, M, N, K, fmt, G):
+    """Problems with too few output tiles for the GPU, where K is split over
+    the CTAs of a cluster and the partial tiles are summed in rank order:
+    exact on integer operands, like the unsplit tiles."""
+    import torch
+
+    assert zq.gemm_plan(M, N, K)[2] > 1, zq.gemm_plan(M, N, K)  # the split path is the one tested
+    r = np.random.default_rng(M * 3 + N + K + fmt)
+    W = _int_weights(r, N, K, G, fmt)
+    X = r.integers(-16, 17, size=(M, K)).astype(np.int64)
+    codes, scales = O.quantize(W.astype(np.float32).ravel(), fmt, G)
+    assert np.all(scales == 1.0)
+    xd = _bf16_dev(_bf16_bits(X.astype(np.float32).ravel()), M, K)
+    want = X.astype(np.float64) @ W.astype(np.float64).T
+    assert np.abs(want).max() < 2 ** 24
+    y = zq.gemm_dequant(xd, bytes_dev(codes), bytes_dev(scales), fmt, G, N)
+    yb = zq.gemm_dequant(xd, bytes_dev(codes), bytes_dev(scales), fmt, G, N, out_dtype=torch.bfloat16)
+    zq.device_status()
+    bad = np.argwhere(to_host(y) != want.astype(np.float32))
+    assert bad.size == 0, f"{len(bad)} outputs differ, first at {bad[:4].tolist()}"
+    assert np.array_equal(to_host(yb), _bf16_bits(want.astype(np.float32).ravel()).reshape(M, N))
+
+
+@pytest.mark.parametrize("M,N,K,fmt,G", [(128, 8192, 8192, O.INT8, 256), (1, 1024, 8192, O.INT4, 128),
+                                         (96, 8192, 28672, O.INT8, 256)])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_gemm_split_k_random_within_bound(zq, M, N, K, fmt, G, out):
+    """Few-token shapes of the Llama-3-70B projections (q / down at 128 and
+    96 tokens, k at one token): random operands, every output of a sampled
+    set against the oracle within the fp32 accumulation bound, which covers
+    the split sum ((p0 + p1) + ...) as well."""
+    import torch
+
+    from blockwise_quantized_zero_gb300 import inputs
+
+    assert zq.gemm_plan(M, N, K)[2] > 1, zq.gemm_plan(M, N, K)
+    w32 = inputs.normal_f32(N * K, 0.02, 210 + fmt, stream=K)
+    codes, scales = O.quantize(w32, fmt, G)
+    xb = _bf16_bits(inputs.normal_f32(M * K, 1.0, 211, stream=M))
+    od = torch.float32 if out == "f32" else torch.bfloat16
+    y = to_host(zq.gemm_dequant(_bf16_dev(xb, M, K), bytes_dev(codes), bytes_dev(scales), fmt, G, N,
+                                out_dtype=od))
+    zq.device_status()
+    r = np.random.default_rng(9)
+    rows = np.concatenate([r.integers(0, M, 2048), np.full(N, M - 1)])
+    cols = np.concatenate([r.integers(0, N, 2048), np.arange(N)])
+    ref, mag = O.gemm_dequant(xb, M, K, codes, scales, fmt, G, N, rows=rows, cols=cols)
+    got = y[rows, cols].astype(np.float64) if out == "f32" else \
+        (y[rows, cols].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    tol = (K / 16) * 2.0 ** -22 * mag + (2.0 ** -8 * np.abs(ref) if out == "bf16" else 0.0)
+    err = np.abs(got - ref)
+    assert np.all(err <= tol), f"worst error {float(np.max(err / np.maximum(tol, 1e-300))):.3f} of the bound"
 
 
 @pytest.mark.parametrize("M,N,K,fmt,G", [(1, 64, 64, O.INT8, 64), (1, 128, 64, O.INT4, 32),
