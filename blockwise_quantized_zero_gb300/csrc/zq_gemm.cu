@@ -516,42 +516,25 @@ int split_ctas_per_wave(int cs) {
 }
 }  // namespace
 
-// Tile shape. Problems of more than 256 rows: the first of 256 x 256,
-// 256 x 128, 128 x 128 whose column width divides N and that still gives
-// every SM an output tile (taller tiles share one dequantized weight tile
-// between more rows), else 128 x 64. (128 x 256 would never come first: a
-// problem it gives enough tiles gives 256 x 128 as many.)
-// Up to 256 rows (few tokens) the tiles are few and the waves of CTAs
-// decide: each candidate, unsplit (persistent) or split-K over clusters of
-// 2, 4 or 8 CTAs (128-row tiles, at least 4 k-blocks a CTA), is given the
-// time waves x (k-blocks a CTA x time a k-block + fixed time a CTA), with
-// the times measured on GB300 (microseconds a 64-deep k-block: 256 x 256
-// 0.885, 256 x 128 0.60, 128 x 256 0.664, 128 x 128 0.49, 128 x 64 0.42;
-// fixed: 3 unsplit, 11 split, which adds the partial-tile exchange), and the
-// fastest is taken.
+// Tile shape and split, from a cost model: each candidate, unsplit
+// (persistent CTAs, 256 x 256, 256 x 128, 128 x 128 or 128 x 64) or, for
+// problems of at most 512 rows, split-K over clusters of 2, 4 or 8 CTAs
+// (128 x 256 or 128 x 128 tiles, at least 4 k-blocks a CTA), is given the
+// time waves x (k-blocks a CTA x time a k-block) + fixed time, with the
+// times measured on GB300 (microseconds a 64-deep k-block: 256 x 256 0.885,
+// 256 x 128 0.60, 128 x 256 0.664, 128 x 128 0.49, 128 x 64 0.42; fixed: 3
+// unsplit, 11 a split CTA, which adds the partial-tile exchange), and the
+// fastest is taken. Waves: tiles / SMs rounded up for the persistent
+// kernels; for clusters, the CTAs over those resident at once.
 void gemm_tile_shape(int64_t M, int64_t N, int64_t K, int &bm, int &bn, int &split) {
   const int64_t sms = device_sm_count();
-  split = 1;
-  if (M > 256) {
-    const int shapes[3][2] = {{256, 256}, {256, 128}, {128, 128}};
-    for (const auto &sh : shapes) {
-      const int64_t tm = (M + sh[0] - 1) / sh[0];
-      if (N % sh[1] == 0 && tm * (N / sh[1]) >= sms) {
-        bm = sh[0];
-        bn = sh[1];
-        return;
-      }
-    }
-    bm = 128;
-    bn = 64;
-    return;
-  }
   const double kb = double(K / kGemmBK);
   struct Unsplit { int bm, bn; double t; };
   const Unsplit us[4] = {{256, 256, 0.885}, {256, 128, 0.60}, {128, 128, 0.49}, {128, 64, 0.42}};
   double best = 1e300;
   bm = 128;
   bn = 64;
+  split = 1;
   for (const auto &u : us) {
     if (N % u.bn != 0) continue;
     const int64_t tiles = (M + u.bm - 1) / u.bm * (N / u.bn);
@@ -562,6 +545,7 @@ void gemm_tile_shape(int64_t M, int64_t N, int64_t K, int &bm, int &bn, int &spl
       bn = u.bn;
     }
   }
+  if (M > 512) return;
   struct Split { int bn; double t; };
   const Split sp[2] = {{256, 0.664}, {128, 0.49}};
   for (const auto &c : sp) {

@@ -13,7 +13,8 @@ Weights are quantized by the oracle (never by the GPU). Two kinds of check:
   (2^-9 |y|, taken as 2^-8) for bf16 output.
 
 Shapes cover each output tile the launcher picks (256 x 256 with one
-accumulator, 256 x 128, 128 x 128 and 128 x 64 with two), several tiles per
+accumulator, 256 x 128, 128 x 128 and 128 x 64 with two; checked through
+zq_gemm_plan), several tiles per
 CTA (the stage ring and the accumulators wrap), a ragged last row tile, every
 code format and several block sizes, and the split-K form for few rows
 (128 x 256 and 128 x 128 tiles over clusters of 2, 4 and 8 CTAs; each case
@@ -98,6 +99,10 @@ BOUND_CASES = [  # tiles 256x128 / 128x64
     (128, 1024, 2048, O.INT4, 32),
     (1000, 1536, 512, O.E4M3, 128),
 ]
+
+
+EDGE_CASES = [(1, 64, 64, O.INT8, 64), (1, 128, 64, O.INT4, 32), (129, 192, 128, O.INT6, 128),
+              (300, 64, 1024, O.INT2, 1024)]
 
 
 @pytest.mark.parametrize("M,N,K,fmt,G", BOUND_CASES)
@@ -195,8 +200,7 @@ def test_gemm_split_k_random_within_bound(zq, M, N, K, fmt, G, out):
     assert np.all(err <= tol), f"worst error {float(np.max(err / np.maximum(tol, 1e-300))):.3f} of the bound"
 
 
-@pytest.mark.parametrize("M,N,K,fmt,G", [(1, 64, 64, O.INT8, 64), (1, 128, 64, O.INT4, 32),
-                                         (129, 192, 128, O.INT6, 128), (300, 64, 1024, O.INT2, 1024)])
+@pytest.mark.parametrize("M,N,K,fmt,G", EDGE_CASES)
 def test_gemm_edge_shapes_exact(zq, M, N, K, fmt, G):
     """One row, the smallest N and K (one k-block), a row tile of one row."""
     r = np.random.default_rng(M * 7 + N + K)
@@ -207,6 +211,18 @@ def test_gemm_edge_shapes_exact(zq, M, N, K, fmt, G):
                         bytes_dev(scales), fmt, G, N)
     zq.device_status()
     assert np.array_equal(to_host(y), (X.astype(np.float64) @ W.astype(np.float64).T).astype(np.float32))
+
+
+def test_gemm_cases_cover_every_plan(zq):
+    """The cases of this file reach every tile the launcher can pick (by its
+    cost model, zq_gemm_plan): 256 x 256, 256 x 128, 128 x 128 and 128 x 64
+    unsplit, and 128 x 256 and 128 x 128 split over clusters of 2, 4 and 8."""
+    cases = EXACT_CASES + BOUND_CASES + EDGE_CASES + SPLIT_CASES
+    plans = {zq.gemm_plan(M, N, K) for M, N, K, _, _ in cases}
+    unsplit = {(bm, bn) for bm, bn, sp in plans if sp == 1}
+    assert {(256, 256), (256, 128), (128, 128), (128, 64)} <= unsplit, plans
+    assert {sp for _, _, sp in plans} >= {2, 4, 8}, plans
+    assert {bn for _, bn, sp in plans if sp > 1} == {128, 256}, plans
 
 
 def test_gemm_empty_problem_enqueues_nothing(zq):
