@@ -63,7 +63,8 @@ __device__ __forceinline__ void put_scale(uint8_t *codes, float *scales, int64_t
 
 // Programmatic dependent launch: wait until the previous grid on the stream
 // has completed and its writes are visible, then let the next grid be
-// scheduled. Every kernel calls this before its first global memory access.
+// scheduled. Every kernel calls this before its first global memory load or
+// store (only an L2 prefetch hint may come earlier: see WarpCursor).
 __device__ __forceinline__ void pdl_enter() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -77,6 +78,21 @@ struct WarpCursor {
     lane = threadIdx.x & 31;
     warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  }
+  // The same, first asking L2 for the warp's first input tile (tile_bytes at
+  // in + warp * tile_bytes, if the warp has a tile): a prefetch is only a
+  // hint, so it may be issued before the previous grid has finished (a
+  // write of that grid to the same bytes still reaches L2 after it).
+  __device__ __forceinline__ WarpCursor(const void *in, int64_t tile_bytes, int64_t ntiles) {
+    lane = threadIdx.x & 31;
+    warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    if (in && warp < ntiles) {
+      const char *p = static_cast<const char *>(in) + warp * tile_bytes;
+      for (int64_t o = int64_t(lane) * 128; o < tile_bytes; o += 32 * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p + o));
+    }
+    pdl_enter();
   }
   // The partial last tile (if any) goes to the warp that would take tile
   // n / kTile in the grid-stride order.
@@ -283,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 3) quantize_kernel(const void *__res
                                                             int64_t n, int wide,
                                                             const SliceRemap rm) {
   static_assert(!IL || FMT != F_E4M3, "the interleaved layout holds integer codes");
-  const WarpCursor c;
+  const WarpCursor c(src, int64_t(kTile) * (DT == DT_F32 ? 4 : 2), n / kTile);
   const int64_t nfull = n / kTile;
   const bool wd = wide != 0;
   __shared__ FixQueue<DT> fq;
@@ -445,7 +461,7 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t *__r
                                                               int log2G, int wide) {
   constexpr int B = Fmt<FMT>::kBits, W = Fmt<FMT>::kWords16;
   static_assert(!IL || FMT != F_E4M3, "the interleaved layout holds integer codes");
-  const WarpCursor c;
+  const WarpCursor c(IL ? nullptr : codes, int64_t(kTile) * B / 8, n / kTile);
   const int64_t nfull = n / kTile;
   const bool wd = wide != 0;
   // Software pipeline: the codes and scales of the warp's next PF tiles are
