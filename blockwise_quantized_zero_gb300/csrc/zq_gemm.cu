@@ -71,16 +71,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc::tmem_alloc(smem_addr(tmem_slot), GG::kTmemCols);
     tc::tmem_relinquish();
   }
+  if (w == 0 && lane == 0) {
+    tc::tma_prefetch_desc(&tm_x);
+    tc::tma_prefetch_desc(&tm_codes);
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // Programmatic dependent launch: the set-up above may overlap the previous
+  // grid's last CTAs; no global memory is read or written before it has
+  // completed (griddepcontrol.wait), and the next grid may be scheduled.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (w == 0) {
     // ---------------- producer: one lane issues the tiled copies ----------------
     if (lane == 0) {
-      tc::tma_prefetch_desc(&tm_x);
-      tc::tma_prefetch_desc(&tm_codes);
       uint32_t u = 0;
       bool ok = true;
       for (int t = t0; t < ntiles && ok; t += tstep) {
@@ -418,24 +425,27 @@ cudaError_t go_gemm(const void *x, const void *codes, const GemmArgs &a, int spl
   if constexpr (SPLIT) {  // one cluster of `split` CTAs per output tile
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = unsigned(split);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(unsigned(tiles * split));
     cfg.blockDim = dim3(kGemmThreads);
     cfg.dynamicSmemBytes = GG::kSmem;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, K, tx, tcd, a);
     return e != cudaSuccess ? e : cudaGetLastError();
   } else {
     (void)split;
     const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
-    K<<<grid, kGemmThreads, GG::kSmem, st>>>(tx, tcd, a);
-    return cudaGetLastError();
+    e = launch_pdl_threads(K, unsigned(grid), unsigned(kGemmThreads), size_t(GG::kSmem), st, tx,
+                           tcd, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
   }
 }
 
