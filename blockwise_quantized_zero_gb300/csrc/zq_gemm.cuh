@@ -12,7 +12,11 @@
 //
 // One persistent CTA per SM walks output tiles of BM x BN (BM = 128 or 256:
 // one or two 128-row MMAs per step on the same weight operand); each k-block
-// is 64 deep. Warp roles (22 warps):
+// is 64 deep. Problems with too few tiles split K over thread-block clusters
+// instead (below). The tile and the split come from a cost model on the
+// host (gemm_tile_shape). Launches use programmatic dependent launch: the
+// set-up runs before griddepcontrol.wait, every global access after it.
+// Warp roles (22 warps):
 //   warp 0      one lane issues the tiled bulk copies (TMA) of the activation
 //               tile (BM x 64 bf16, 128-byte swizzled) and of the packed code
 //               tile (BN rows x 64 codes) into a stage of shared memory;
