@@ -275,6 +275,55 @@ def test_gemm_plan(L):
     assert p(1, 64, 64, *out) == OK and (bm.value, bn.value, sp.value) == (128, 64, 1)
 
 
+def _plan_model(M, N, K, sms, wave):
+    """The tile cost model of zq_gemm_dequant as its source comment states it:
+    waves x (k-blocks a CTA x time a k-block) + fixed time, over the unsplit
+    persistent shapes and, up to 512 rows, split-K over clusters of 2, 4, 8."""
+    kb = K // 64
+    best, plan = float("inf"), (128, 64, 1)
+    for bm, bn, t in ((256, 256, 0.885), (256, 128, 0.60), (128, 128, 0.49), (128, 64, 0.42)):
+        if N % bn:
+            continue
+        tiles = -(-M // bm) * (N // bn)
+        cost = -(-tiles // sms) * (kb * t) + 3.0
+        if cost < best:
+            best, plan = cost, (bm, bn, 1)
+    if M <= 512:
+        for bn, t in ((256, 0.664), (128, 0.49)):
+            if N % bn:
+                continue
+            tiles = -(-M // 128) * (N // bn)
+            for cs in (2, 4, 8):
+                if kb < 4 * cs:
+                    continue
+                cost = -(-(tiles * cs) // wave(cs)) * (kb / cs * t + 11.0)
+                if cost < best:
+                    best, plan = cost, (128, bn, cs)
+    return plan
+
+
+def test_gemm_plan_follows_the_cost_model(L):
+    """Without a device the launcher plans with its fallback SM count (148)
+    and cluster waves (148 // cs * cs); its choice must be the documented cost
+    model's on a spread of shapes (few tokens to large problems, every tile
+    and split)."""
+    I = ctypes.c_int
+    p = L.zq_gemm_plan
+    p.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(I), ctypes.POINTER(I),
+                  ctypes.POINTER(I)]
+    bm, bn, sp = I(), I(), I()
+    checked = set()
+    for M in (1, 16, 77, 128, 200, 256, 300, 512, 513, 1024, 2148, 4096, 8192):
+        for N in (64, 192, 512, 1024, 1536, 2560, 4096, 8192, 28672):
+            for K in (64, 512, 2048, 8192, 28672):
+                assert p(M, N, K, ctypes.byref(bm), ctypes.byref(bn), ctypes.byref(sp)) == OK
+                want = _plan_model(M, N, K, 148, lambda cs: 148 // cs * cs)
+                assert (bm.value, bn.value, sp.value) == want, (M, N, K, want)
+                checked.add(want)
+    assert {(256, 256, 1), (256, 128, 1), (128, 128, 1), (128, 64, 1)} <= checked
+    assert {s for _, _, s in checked} >= {1, 2, 4, 8}
+
+
 def test_quantize_multi_argument_errors(L):
     """zq_quantize_multi: bad format / type, negative counts and sizes, null,
     misaligned and overlapping buffers are refused before any work."""
