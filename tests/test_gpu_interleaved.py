@@ -1,8 +1,8 @@
 """Aquavit's metadata-interleaved record layout on the GPU (through the C ABI)
 against the oracle, bit for bit: the record stream of the quantize kernel and
 the values of the dequantize kernel, for every integer width, block size and
-element type, ragged sizes, and the full 8192x8192 bf16 shard on sampled
-windows of whole blocks."""
+element type, ragged sizes, and the full 8192x8192 bf16 shard on every
+element."""
 import numpy as np
 import pytest
 
