@@ -1852,7 +1852,10 @@ def csrc_sha(sset: str = "gemm") -> str:
     return h.hexdigest()[:16]
 
 
-def main(argv=None):
+def parse_args(argv=None):
+    """The command line, checked: at least 3 warm-up steps for the GPU arm,
+    and the options that serve one workload (--pair, --schedule-steps) only
+    with that workload."""
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
@@ -1873,6 +1876,22 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "zq":
         ap.error("at least 3 warm-up steps")
+    if args.pair is not None:
+        if args.workload != "gm_sweep":
+            ap.error("--pair applies to --workload gm_sweep only")
+        try:
+            b, G = (int(v) for v in args.pair.split(":"))
+        except ValueError:
+            ap.error("--pair takes b:G, for example 4:128")
+        if b not in (2, 4, 6, 8) or G not in (32, 64, 128, 256, 512, 1024):
+            ap.error("--pair: b in {2, 4, 6, 8} and G a power of two in [32, 1024]")
+    if args.schedule_steps is not None and args.workload != "aquavit_schedule":
+        ap.error("--schedule-steps applies to --workload aquavit_schedule only")
+    return args
+
+
+def main(argv=None):
+    args = parse_args(argv)
     rank, world, local = dist_init()
     if args.impl == "reference":
         line = run_reference(args, rank, world)
