@@ -143,6 +143,38 @@ def test_e4m3_conversion_exhaustive_near_midpoints(zq):
     assert_same_codes(codes, want_c, "e4m3")
 
 
+def test_e4m3_conversion_every_binary32_to_448(zq):
+    """The same scale-1 blocks over every binary32 value whose magnitude lies
+    in [2^-11, 448], both signs (331,350,018 values; every smaller magnitude
+    is below half the smallest E4M3 subnormal, 2^-10), every binary32
+    subnormal and zero, and 2^24 seeded samples of the normal range below
+    2^-11: all against the oracle's conversion, on every host core."""
+    import time
+
+    import fullsize as F
+
+    t0 = time.time()
+    G = 128
+    mag = np.concatenate([
+        np.arange(0x3A000000, 0x43E00000 + 1, dtype=np.uint32),  # 2^-11 .. 448
+        np.arange(0, 0x00800000, dtype=np.uint32),  # zero and the subnormals
+        np.random.default_rng(11).integers(0x00800000, 0x3A000000, 1 << 24, dtype=np.uint32)])
+    vals = np.concatenate([mag, mag | np.uint32(0x80000000)]).view(np.float32)
+    del mag
+    nb = -(-vals.size // (G - 1))
+    x = np.zeros((nb, G), np.float32)
+    x[:, 0] = 448.0
+    x[:, 1:] = np.concatenate([vals, np.zeros(nb * (G - 1) - vals.size, np.float32)]).reshape(nb, G - 1)
+    x = x.reshape(-1)
+    del vals
+    codes, scales = gpu_quantize(zq, x, O.F32, O.E4M3, G)
+    assert np.all(scales == 1.0)
+    n = F.check_roundtrip("e4m3 conversion", x, O.F32, O.E4M3, G, codes, scales)
+    assert n == x.size
+    print(f"\n[e4m3] {n:,} elements (every binary32 in [2^-11, 448] of both signs among them) "
+          f"compared on {F.cores()} host cores in {time.time() - t0:.1f} s")
+
+
 def test_quantize_subnormal_scales(zq):
     """bf16 subnormal inputs give subnormal scales; the exact path (with its
     clamp) must agree with the definition."""
